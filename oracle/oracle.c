@@ -1,0 +1,341 @@
+/*
+ * oracle.c -- plain, slow, obviously-correct CPU oracle for the GGUF
+ * quantized-weight prefill GEMM  Y[M,N] = X[M,K] . W[N,K]^T.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The product path
+ * (the CUDA library) shares no code, header, table or helper with it.
+ *
+ * What it computes, and the passage each part follows:
+ *
+ *  O1  binary16 <-> binary32 conversion, written from the IEEE 754 binary16
+ *      definition: round-to-nearest-even, gradual underflow, signed zeros.
+ *      The pages round every dequantized value through __float2half, which
+ *      is round-to-nearest-even ("05 · 8p — Persistent f16 weight cache +
+ *      fused dequant-in-GEMM", section 3.3 Pitfalls: the same rounding path).
+ *
+ *  O2  Block decoders Q8_0 / Q4_K / Q6_K -> binary16.  The pages name the
+ *      types and their bytes per weight only ("05 · 8p", section 1); the
+ *      block sizes 34 / 144 / 210 bytes and the field layout follow the
+ *      GGUF format convention (a reading: no page prints the layout).
+ *      Arithmetic is binary32 in the fixed order d*sc*q - dmin*m, then one
+ *      round-to-nearest to binary16, as the dequant kernel shown in
+ *      "05 · 8p", section 3.2 does (f32 product, then __float2half).
+ *      The weight is one flat stream of N*K elements in consecutive blocks;
+ *      element (n,k) is flat index n*K+k, so a row may start inside a block.
+ *
+ *  O4  GEMM with f64 accumulation in k order: Y[m,n] = sum_k X[m,k]*W[n,k]
+ *      for f16 X and the f16 dequantized W, the product the pages check
+ *      their kernels against ("Eager GPU Offload Without A Compute Graph",
+ *      section "F16 and GGUF quantized linears": an explicitly dequantized
+ *      reference).
+ *
+ * Build: gcc -O2 -ffp-contract=off -fno-fast-math -fopenmp -shared -fPIC.
+ * Contraction stays off so every binary32 product and difference is
+ * rounded exactly where the C source says.
+ */
+#include <stdint.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ */
+/* O1: binary16 <-> binary32                                          */
+/* ------------------------------------------------------------------ */
+
+/* binary16 -> binary32, exact: a normal value is (1024+m) * 2^(e-25), a
+ * subnormal one m * 2^-24. */
+float oracle_f16_to_f32(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0x1f) {
+        if (m != 0) return sign ? -NAN : NAN;
+        v = INFINITY;
+    } else if (e == 0) {
+        v = ldexp((double)m, -24);
+    } else {
+        v = ldexp((double)(m + 1024), e - 25);
+    }
+    return (float)(sign ? -v : v);
+}
+
+/* binary32 -> binary16, round to nearest, ties to even.
+ * The binary32 value is sig * 2^(e-23) with sig its 24-bit significand
+ * (implicit bit included for normals).  The binary16 quantum at that
+ * magnitude is 2^(max(e,-14)-10), so 13 + max(-14-e, 0) low bits of sig
+ * are rounded away, leaving q.  A normal result encodes as
+ * ((e+15)<<10) + (q-1024): a carry out of the significand lands in the
+ * exponent field by itself.  A subnormal result encodes as q (q == 1024 is
+ * the smallest normal).  Encodings >= 0x7c00 overflow to infinity.  NaNs
+ * stay NaNs (quiet bit set, top payload bits kept). */
+uint16_t oracle_f32_to_f16(float f)
+{
+    uint32_t x;
+    memcpy(&x, &f, 4);
+    uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    int ex = (int)((x >> 23) & 0xff);
+    uint32_t man = x & 0x7fffffu;
+
+    if (ex == 0xff)
+        return man ? (uint16_t)(sign | 0x7e00u | (man >> 13)) : (uint16_t)(sign | 0x7c00u);
+
+    uint64_t sig = ex ? (man | 0x800000u) : man;
+    int e = ex ? ex - 127 : -126;
+    if (e >= 16)
+        return (uint16_t)(sign | 0x7c00u);
+
+    int shift = 13 + (e < -14 ? -14 - e : 0);
+    uint64_t q = 0;
+    if (shift < 40) {
+        uint64_t rem = sig & ((1ull << shift) - 1);
+        uint64_t half = 1ull << (shift - 1);
+        q = sig >> shift;
+        if (rem > half || (rem == half && (q & 1)))
+            q++;
+    }
+    uint32_t enc = (e < -14) ? (uint32_t)q
+                             : (uint32_t)((e + 15) << 10) + (uint32_t)(q - 1024);
+    if (enc >= 0x7c00u)
+        enc = 0x7c00u;
+    return (uint16_t)(sign | enc);
+}
+
+/* ------------------------------------------------------------------ */
+/* O2: block decoders                                                 */
+/* ------------------------------------------------------------------ */
+
+enum { T_Q8_0 = 8, T_Q4_K = 12, T_Q6_K = 14 };
+
+static uint16_t rd_u16le(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* Q8_0, 34 bytes: d (f16) at byte 0, q[32] (int8) at byte 2.
+ * y_e = RN16(d * q_e). */
+static void decode_q8_0_block(const uint8_t *b, uint16_t *y)
+{
+    float d = oracle_f16_to_f32(rd_u16le(b));
+    for (int e = 0; e < 32; e++) {
+        float q = (float)(int8_t)b[2 + e];
+        y[e] = oracle_f32_to_f16(d * q);
+    }
+}
+
+/* Q4_K 6-bit scale and min of sub-block s (0..7) from the 12 packed bytes S:
+ *   s <  4: sc = S[s] & 63,                         m = S[s+4] & 63
+ *   s >= 4: sc = (S[s+4] & 15) | (S[s-4] >> 6) << 4, m = (S[s+4] >> 4) | (S[s] >> 6) << 4 */
+static void q4k_scale_min(const uint8_t *S, int s, int *sc, int *m)
+{
+    if (s < 4) {
+        *sc = S[s] & 63;
+        *m = S[s + 4] & 63;
+    } else {
+        *sc = (S[s + 4] & 15) | ((S[s - 4] >> 6) << 4);
+        *m = (S[s + 4] >> 4) | ((S[s] >> 6) << 4);
+    }
+}
+
+/* Q4_K, 144 bytes: d (f16) at 0, dmin (f16) at 2, S[12] at 4, qs[128] at 16.
+ * Group p = 0..3 covers elements 64p .. 64p+63: element 64p+i (i < 32) is
+ * the low nibble of qs[32p+i] and belongs to sub-block 2p; element
+ * 64p+32+i is the high nibble of the same byte, sub-block 2p+1.
+ *   y = RN16( RN32( RN32(RN32(d*sc)*q) - RN32(dmin*m) ) ) */
+static void decode_q4_K_block(const uint8_t *b, uint16_t *y)
+{
+    float d = oracle_f16_to_f32(rd_u16le(b));
+    float dmin = oracle_f16_to_f32(rd_u16le(b + 2));
+    const uint8_t *S = b + 4;
+    const uint8_t *qs = b + 16;
+    for (int e = 0; e < 256; e++) {
+        int p = e / 64;
+        int hi = (e % 64) >= 32;
+        int i = e % 32;
+        int s = 2 * p + hi;
+        int q = hi ? (qs[32 * p + i] >> 4) : (qs[32 * p + i] & 15);
+        int sc, m;
+        q4k_scale_min(S, s, &sc, &m);
+        float a = (d * (float)sc) * (float)q;
+        float c = dmin * (float)m;
+        y[e] = oracle_f32_to_f16(a - c);
+    }
+}
+
+/* Q6_K, 210 bytes: ql[128] at 0, qh[64] at 128, sc[16] (int8) at 192,
+ * d (f16) at 208.  Half h (0,1) covers elements 128h .. 128h+127 and reads
+ * L = ql + 64h, H = qh + 32h.  For l = 0..31:
+ *   element 128h + l      : (L[l]    & 15) | ((H[l] >> 0) & 3) << 4
+ *   element 128h + l + 32 : (L[l+32] & 15) | ((H[l] >> 2) & 3) << 4
+ *   element 128h + l + 64 : (L[l]    >> 4) | ((H[l] >> 4) & 3) << 4
+ *   element 128h + l + 96 : (L[l+32] >> 4) | ((H[l] >> 6) & 3) << 4
+ * q6 = value - 32, its scale is sc[e/16], and
+ *   y = RN16( RN32(RN32(d*sc)*q6) ) */
+static void decode_q6_K_block(const uint8_t *b, uint16_t *y)
+{
+    const uint8_t *ql = b;
+    const uint8_t *qh = b + 128;
+    const int8_t *sc = (const int8_t *)(b + 192);
+    float d = oracle_f16_to_f32(rd_u16le(b + 208));
+    for (int e = 0; e < 256; e++) {
+        int h = e / 128;
+        int r = e % 128;
+        int quarter = r / 32;
+        int l = r % 32;
+        const uint8_t *L = ql + 64 * h;
+        const uint8_t *H = qh + 32 * h;
+        int lo, hb;
+        switch (quarter) {
+        case 0:  lo = L[l] & 15;       hb = (H[l] >> 0) & 3; break;
+        case 1:  lo = L[l + 32] & 15;  hb = (H[l] >> 2) & 3; break;
+        case 2:  lo = L[l] >> 4;       hb = (H[l] >> 4) & 3; break;
+        default: lo = L[l + 32] >> 4;  hb = (H[l] >> 6) & 3; break;
+        }
+        int q6 = (lo | (hb << 4)) - 32;
+        float s = (float)sc[e / 16];
+        y[e] = oracle_f32_to_f16((d * s) * (float)q6);
+    }
+}
+
+/* Elements per block (QK) and bytes per block for a GGUF type id. */
+int oracle_block_size(int type, int *qk, int *bytes)
+{
+    switch (type) {
+    case T_Q8_0: *qk = 32;  *bytes = 34;  return 0;
+    case T_Q4_K: *qk = 256; *bytes = 144; return 0;
+    case T_Q6_K: *qk = 256; *bytes = 210; return 0;
+    default: return -1;
+    }
+}
+
+/* Decode nblocks consecutive blocks of one flat stream into nblocks*QK
+ * binary16 values (raw bits) in stream order.  For a weight W[N,K] stored
+ * as one stream, out is W row-major with row stride K. */
+int oracle_decode(int type, const uint8_t *q, int64_t nblocks, uint16_t *out)
+{
+    int qk, bb;
+    if (oracle_block_size(type, &qk, &bb))
+        return -1;
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < nblocks; i++) {
+        const uint8_t *b = q + i * bb;
+        uint16_t *y = out + i * qk;
+        if (type == T_Q8_0)
+            decode_q8_0_block(b, y);
+        else if (type == T_Q4_K)
+            decode_q4_K_block(b, y);
+        else
+            decode_q6_K_block(b, y);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* O4: GEMM with f64 accumulation                                     */
+/* ------------------------------------------------------------------ */
+
+static void widen_row(const uint16_t *src, int64_t K, double *dst)
+{
+    for (int64_t k = 0; k < K; k++)
+        dst[k] = (double)oracle_f16_to_f32(src[k]);
+}
+
+static double dot_f64(const double *x, const double *w, int64_t K)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; k++)
+        acc += x[k] * w[k];
+    return acc;
+}
+
+/* Y[m*N + n] = sum_{k=0}^{K-1} X[m*K + k] * W[n*K + k], X [M,K] and W [N,K]
+ * as f16 bits, every product and partial sum in double, k increasing. */
+int oracle_gemm_f64(const uint16_t *X, int64_t M, int64_t K,
+                    const uint16_t *W, int64_t N, double *Y)
+{
+    double *xd = (double *)malloc((size_t)(M * K > 0 ? M * K : 1) * sizeof(double));
+    if (!xd)
+        return -2;
+    #pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; m++)
+        widen_row(X + m * K, K, xd + m * K);
+
+    int err = 0;
+    #pragma omp parallel
+    {
+        double *wd = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+        if (!wd) {
+            #pragma omp atomic write
+            err = 1;
+        }
+        #pragma omp for schedule(dynamic, 4)
+        for (int64_t n = 0; n < N; n++) {
+            if (!wd)
+                continue;
+            widen_row(W + n * K, K, wd);
+            for (int64_t m = 0; m < M; m++)
+                Y[m * N + n] = dot_f64(xd + m * K, wd, K);
+        }
+        free(wd);
+    }
+    free(xd);
+    return err ? -2 : 0;
+}
+
+/* The same sum for `count` chosen (m, n) pairs only: out[i] is Y[mi[i], ni[i]].
+ * Lets a test check a full-size GEMM at sampled outputs. */
+int oracle_gemm_f64_sampled(const uint16_t *X, int64_t K, const uint16_t *W,
+                            const int64_t *mi, const int64_t *ni, int64_t count,
+                            double *out)
+{
+    int err = 0;
+    #pragma omp parallel
+    {
+        double *xd = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+        double *wd = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+        if (!xd || !wd) {
+            #pragma omp atomic write
+            err = 1;
+        }
+        #pragma omp for schedule(dynamic, 16)
+        for (int64_t i = 0; i < count; i++) {
+            if (!xd || !wd)
+                continue;
+            widen_row(X + mi[i] * K, K, xd);
+            widen_row(W + ni[i] * K, K, wd);
+            out[i] = dot_f64(xd, wd, K);
+        }
+        free(xd);
+        free(wd);
+    }
+    return err ? -2 : 0;
+}
+
+/* Number of OpenMP threads a parallel region of this library uses. */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Element-wise array forms of O1, for tests and input preparation. */
+void oracle_f32_to_f16_n(const float *src, int64_t n, uint16_t *dst)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; i++)
+        dst[i] = oracle_f32_to_f16(src[i]);
+}
+
+void oracle_f16_to_f32_n(const uint16_t *src, int64_t n, float *dst)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; i++)
+        dst[i] = oracle_f16_to_f32(src[i]);
+}

@@ -1,0 +1,145 @@
+"""Seeded synthetic inputs: GGUF-style quantized weights and f16 activations.
+
+This module only draws random numbers and lays them into block bytes at the
+fields' byte offsets.  It holds none of the method's arithmetic (no
+decoding, no GEMM) and imports neither the CUDA library nor the oracle, so
+both sides can be fed the same bytes.
+
+Recipe (numpy ``Generator(PCG64(seed))``, one generator per workload, weights
+drawn in the listed order, then the activations):
+
+* Q4_K block (144 B): d ~ U[2e-4, 1e-3] and dmin ~ U[0, 5e-4], each rounded
+  to f16 and stored little-endian at bytes 0 and 2; the 12 packed scale/min
+  bytes and the 128 nibble bytes are uniform random bytes, so every 6-bit
+  scale and min is uniform on {0..63} and every nibble on {0..15}.
+* Q6_K block (210 B): ql (128 B) and qh (64 B) uniform bytes, 16 int8 scales
+  uniform on {-128..127}, d ~ U[2e-4, 1e-3] as f16 at byte 208.
+* Q8_0 block (34 B): d ~ U[1e-3, 5e-3] as f16 at byte 0, 32 int8 quants
+  uniform on {-127..127}.
+* Activations X[M,K] ~ N(0,1) in f32, rounded to f16.
+
+Draw order inside a weight: Q4_K d, dmin, scale bytes, nibble bytes;
+Q6_K ql, qh, scales, d; Q8_0 d, quants.  Field values are drawn for all
+blocks of the weight at once.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+Q8_0, Q4_K, Q6_K = 8, 12, 14
+BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
+TYPE_NAME = {Q8_0: "q8_0", Q4_K: "q4_K", Q6_K: "q6_K"}
+
+
+def rng(seed: int = 0) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def _f16_le_bytes(v: np.ndarray) -> np.ndarray:
+    """[n] float values -> [n, 2] little-endian f16 bytes."""
+    return v.astype(np.float16).astype("<f2").view(np.uint8).reshape(-1, 2)
+
+
+def q4_K_blocks(g: np.random.Generator, nblocks: int) -> np.ndarray:
+    d = g.uniform(2e-4, 1e-3, nblocks)
+    dmin = g.uniform(0.0, 5e-4, nblocks)
+    scales = g.integers(0, 256, (nblocks, 12), dtype=np.uint8)
+    qs = g.integers(0, 256, (nblocks, 128), dtype=np.uint8)
+    b = np.empty((nblocks, 144), dtype=np.uint8)
+    b[:, 0:2] = _f16_le_bytes(d)
+    b[:, 2:4] = _f16_le_bytes(dmin)
+    b[:, 4:16] = scales
+    b[:, 16:144] = qs
+    return b.reshape(-1)
+
+
+def q6_K_blocks(g: np.random.Generator, nblocks: int) -> np.ndarray:
+    ql = g.integers(0, 256, (nblocks, 128), dtype=np.uint8)
+    qh = g.integers(0, 256, (nblocks, 64), dtype=np.uint8)
+    sc = g.integers(-128, 128, (nblocks, 16), dtype=np.int16).astype(np.int8)
+    d = g.uniform(2e-4, 1e-3, nblocks)
+    b = np.empty((nblocks, 210), dtype=np.uint8)
+    b[:, 0:128] = ql
+    b[:, 128:192] = qh
+    b[:, 192:208] = sc.view(np.uint8)
+    b[:, 208:210] = _f16_le_bytes(d)
+    return b.reshape(-1)
+
+
+def q8_0_blocks(g: np.random.Generator, nblocks: int) -> np.ndarray:
+    d = g.uniform(1e-3, 5e-3, nblocks)
+    q = g.integers(-127, 128, (nblocks, 32), dtype=np.int16).astype(np.int8)
+    b = np.empty((nblocks, 34), dtype=np.uint8)
+    b[:, 0:2] = _f16_le_bytes(d)
+    b[:, 2:34] = q.view(np.uint8)
+    return b.reshape(-1)
+
+
+_DRAW = {Q4_K: q4_K_blocks, Q6_K: q6_K_blocks, Q8_0: q8_0_blocks}
+
+
+def nblocks(qtype: int, N: int, K: int) -> int:
+    qk, _ = BLOCK[qtype]
+    if (N * K) % qk:
+        raise ValueError(f"N*K={N * K} is not a whole number of {qk}-element blocks")
+    return N * K // qk
+
+
+def weight_bytes(g: np.random.Generator, qtype: int, N: int, K: int) -> np.ndarray:
+    """Flat block stream of a weight W[N,K] (element (n,k) = flat n*K+k)."""
+    return _DRAW[qtype](g, nblocks(qtype, N, K))
+
+
+def activations(g: np.random.Generator, M: int, K: int) -> np.ndarray:
+    """X[M,K] ~ N(0,1) rounded to f16 (numpy float16 array)."""
+    return g.standard_normal((M, K), dtype=np.float32).astype(np.float16)
+
+
+@dataclass
+class Weight:
+    name: str
+    qtype: int
+    N: int
+    K: int
+    data: np.ndarray  # uint8 flat block stream
+
+
+# Layer shapes (name, type, N rows = output features, K = input features).
+QWEN25_7B = [("q", Q4_K, 3584, 3584), ("k", Q4_K, 512, 3584), ("v", Q4_K, 512, 3584),
+             ("o", Q4_K, 3584, 3584), ("gate", Q4_K, 18944, 3584),
+             ("up", Q4_K, 18944, 3584), ("down", Q6_K, 3584, 18944)]
+LLAMA31_8B = [("q", Q4_K, 4096, 4096), ("k", Q4_K, 1024, 4096), ("v", Q4_K, 1024, 4096),
+              ("o", Q4_K, 4096, 4096), ("gate", Q4_K, 14336, 4096),
+              ("up", Q4_K, 14336, 4096), ("down", Q4_K, 4096, 14336)]
+Q8_0_PAIR = [("w1", Q8_0, 3584, 18944), ("w2", Q8_0, 18944, 3584)]
+SINGLE_896 = [("w", Q4_K, 896, 896)]
+
+WORKLOADS = {
+    # name: (weights, token counts M)
+    "q4k_896": (SINGLE_896, [128]),
+    "qwen2.5-7b_layer": (QWEN25_7B, [2048]),
+    "llama3.1-8b_layer": (LLAMA31_8B, [512]),
+    "q8_0_pair": (Q8_0_PAIR, [128, 1024]),
+    "small_m_sweep": ([w for w in QWEN25_7B if w[0] in ("gate", "up", "down")],
+                      [1, 8, 32, 128, 512, 2048]),
+}
+
+
+def workload(name: str, seed: int = 0, max_m: int | None = None):
+    """Weights of a named workload and one activation matrix per distinct K.
+
+    Returns (weights, xs) where xs maps K -> X[max(M), K] (f16).  Smaller M
+    use the leading rows.  Draw order: every weight in list order, then one
+    X per distinct K in order of first appearance.
+    """
+    shapes, ms = WORKLOADS[name]
+    g = rng(seed)
+    weights = [Weight(n, t, N, K, weight_bytes(g, t, N, K)) for (n, t, N, K) in shapes]
+    M = max_m if max_m is not None else max(ms)
+    xs = {}
+    for w in weights:
+        if w.K not in xs:
+            xs[w.K] = activations(g, M, w.K)
+    return weights, xs

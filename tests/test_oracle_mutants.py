@@ -1,0 +1,63 @@
+"""Each pin set must catch plausible mistakes in the oracle.
+
+Every mutant below is a copy of the oracle's C source with one plausible
+mistake planted by text substitution (on the CPU, in a temporary directory;
+the oracle itself is untouched).  The test compiles the mutant and runs all
+pins against it: at least one pin must fail, or the pins are too weak.
+"""
+import os
+import shutil
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+SRC = os.path.dirname(os.path.abspath(oracle.__file__))
+
+MUTANTS = {
+    "f16_ties_away": ("if (rem > half || (rem == half && (q & 1)))", "if (rem >= half)"),
+    "f16_truncate": ("if (rem > half || (rem == half && (q & 1)))", "if (0)"),
+    "f16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    "f16_no_subnormals": ("uint32_t enc = (e < -14) ? (uint32_t)q", "uint32_t enc = (e < -14) ? 0u"),
+    "q8_0_unsigned_quants": ("float q = (float)(int8_t)b[2 + e];", "float q = (float)b[2 + e];"),
+    "q4k_nibbles_swapped": ("int q = hi ? (qs[32 * p + i] >> 4) : (qs[32 * p + i] & 15);",
+                            "int q = hi ? (qs[32 * p + i] & 15) : (qs[32 * p + i] >> 4);"),
+    "q4k_wrong_subblock": ("q4k_scale_min(S, s, &sc, &m);", "q4k_scale_min(S, s ^ 1, &sc, &m);"),
+    "q4k_high_scale_bits": ("*sc = (S[s + 4] & 15) | ((S[s - 4] >> 6) << 4);",
+                            "*sc = (S[s + 4] & 15) | ((S[s] >> 6) << 4);"),
+    "q4k_min_uses_d": ("float c = dmin * (float)m;", "float c = d * (float)m;"),
+    "q4k_sign_flipped": ("y[e] = oracle_f32_to_f16(a - c);", "y[e] = oracle_f32_to_f16(c - a);"),
+    "q4k_min_dropped": ("y[e] = oracle_f32_to_f16(a - c);", "y[e] = oracle_f32_to_f16(a);"),
+    "q4k_group_stride": ("int p = e / 64;", "int p = e / 32 % 4;"),
+    "q6k_ql_half_swapped": ("case 2:  lo = L[l] >> 4; ", "case 2:  lo = L[l + 32] >> 4; "),
+    "q6k_qh_shift": ("case 1:  lo = L[l + 32] & 15;  hb = (H[l] >> 2) & 3;",
+                     "case 1:  lo = L[l + 32] & 15;  hb = (H[l] >> 4) & 3;"),
+    "q6k_scale_per_32": ("float s = (float)sc[e / 16];", "float s = (float)sc[e / 32];"),
+    "q6k_offset": ("int q6 = (lo | (hb << 4)) - 32;", "int q6 = (lo | (hb << 4)) - 31;"),
+    "q6k_unsigned_scale": ("const int8_t *sc = (const int8_t *)(b + 192);",
+                           "const uint8_t *sc = (const uint8_t *)(b + 192);"),
+    "gemm_reversed_operand": ("acc += x[k] * w[k];", "acc += x[k] * w[K - 1 - k];"),
+    "gemm_f32_accumulator": ("double acc = 0.0;", "float acc = 0.0f;"),
+    "gemm_drops_last_term": ("for (int64_t k = 0; k < K; k++)\n        acc += x[k] * w[k];",
+                             "for (int64_t k = 0; k + 1 < K; k++)\n        acc += x[k] * w[k];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    for s in oracle.SOURCES:
+        shutil.copy(os.path.join(SRC, s), tmp_path / s)
+    src = (tmp_path / "oracle.c").read_text()
+    assert src.count(old) == 1, f"mutation site not found exactly once: {old!r}"
+    (tmp_path / "oracle.c").write_text(src.replace(old, new))
+    lib = oracle.build(out=str(tmp_path / "libmutant.so"), src_dir=str(tmp_path))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutant {name}"
