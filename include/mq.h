@@ -1,0 +1,206 @@
+/*
+ * mq.h -- C ABI of the GB300 (sm_103a) quantized-weight prefill GEMM library.
+ *
+ * Computes the prefill matmul Y[M,N] = X[M,K] . W[N,K]^T where X is f16
+ * activations, W is a GGUF block-quantized weight (Q4_K, Q6_K or Q8_0) and Y
+ * is f32.  Two ways, both from the pages:
+ *
+ *   cached  W is decoded once, at registration, into a persistent f16 copy
+ *           that a tensor-core GEMM then reads ("05 · 8p — Persistent f16
+ *           weight cache + fused dequant-in-GEMM", sections 1-2; "ggml-cuda:
+ *           GEMM weight row padding + one-time K-padded f16 dequant for
+ *           prefill", Summary: the load-time K-padded f16 shadow).
+ *   fused   the GEMM stages the raw quantized blocks on chip and decodes them
+ *           to f16 right before the MMA ("05 · 8p", section 2, fused
+ *           dequant-in-GEMM; section 3.2, third site).
+ *
+ * and an M gate that picks one per call ("ggml-cuda: GEMM weight row
+ * padding ...", Summary: the token-count threshold GGML_PREFILL_DEQUANT).
+ *
+ * Conventions for every function below:
+ *  - Return value: MQ_OK (0) or a negative MQ_ERR_* code.  No call aborts the
+ *    process and no call falls back to the CPU.  mq_last_error_detail()
+ *    names the argument and the reason of the last failure on this thread.
+ *  - Pointers named x, y, qdata, out_f16 are DEVICE pointers owned by the
+ *    caller; they must stay valid until the stream work that uses them has
+ *    completed.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ *  - All device work is enqueued on `stream` in call order; no function
+ *    except mq_stream_status() and mq_release_weight() synchronizes.
+ *  - Layouts are row-major: X[M,K] with row stride K elements, Y[M,N] with
+ *    row stride N elements.
+ *  - Decoded weights match the block definitions bit for bit: each value is
+ *    computed in f32 as d*sc*q - dmin*m (Q4_K), d*sc*q (Q6_K) or d*q (Q8_0)
+ *    and rounded once to nearest-even f16 (the dequant kernel of "05 · 8p",
+ *    section 3.2: f32 product, then __float2half).  The cached and the fused
+ *    paths decode to identical f16 values (section 3.3 Pitfalls: the same
+ *    rounding path).
+ */
+#ifndef MQ_H
+#define MQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* GGUF type ids of the supported block formats. */
+typedef enum {
+    MQ_TYPE_Q8_0 = 8,   /* 32 elements in 34 bytes: f16 d, int8 q[32]                 */
+    MQ_TYPE_Q4_K = 12,  /* 256 elements in 144 bytes: f16 d, f16 dmin, 12 B of 6-bit
+                           scales/mins, 128 B of 4-bit quants                          */
+    MQ_TYPE_Q6_K = 14   /* 256 elements in 210 bytes: 128 B low nibbles, 64 B high
+                           2-bit fields, 16 int8 scales, f16 d                          */
+} mq_type;
+
+/* Status codes. */
+#define MQ_OK                    0
+#define MQ_ERR_INVALID          -1  /* null pointer, unknown or released handle, bad flag  */
+#define MQ_ERR_UNSUPPORTED_TYPE -2  /* type id is not Q8_0 / Q4_K / Q6_K                  */
+#define MQ_ERR_SHAPE            -3  /* a size precondition does not hold                   */
+#define MQ_ERR_ALIGN            -4  /* a pointer is not 16-byte aligned                    */
+#define MQ_ERR_NO_CACHE         -5  /* mq_gemm on a handle registered with MQ_REG_NO_CACHE */
+#define MQ_ERR_OOM              -6  /* device allocation failed                            */
+#define MQ_ERR_CUDA             -7  /* a CUDA runtime/driver call failed (detail has it)   */
+#define MQ_ERR_DEVICE           -8  /* a kernel flagged a device-side error (timeout)      */
+#define MQ_ERR_NO_DEVICE        -9  /* no usable sm_103 device / kernel image              */
+
+/* Registration flags. */
+#define MQ_REG_NO_CACHE 0x1u  /* build no f16 cache: only fused calls on this handle     */
+#define MQ_REG_NO_KPAD  0x2u  /* cache row stride ldk = K even when 2K % 2048 == 0       */
+#define MQ_REG_KPAD     0x4u  /* force ldk = K + 64                                      */
+
+typedef struct mq_weight *mq_handle;
+
+/*
+ * mq_register_weight -- take a quantized weight and (unless MQ_REG_NO_CACHE)
+ * decode it once into a persistent f16 cache.
+ *
+ * Passage: "05 · 8p", section 3.1 (dequantize at load in the warm pass, the
+ * f16 copy stays resident) and section 2 (weights are immutable after load,
+ * so the pointer can key the cache); "ggml-cuda: GEMM weight row padding ...",
+ * Summary (the shadow is K-padded by one 128-byte line only when its f16 row
+ * size is a multiple of 2048 bytes; allocation failure is reported at load,
+ * Known limitation).
+ *
+ *  type   block format.
+ *  qdata  device pointer to ONE flat stream of N*K/QK consecutive blocks;
+ *         element (n,k) is flat element n*K+k (rows may start inside a
+ *         block when K % QK != 0).  16-byte aligned.  Caller-owned: it must
+ *         stay valid and UNCHANGED for the lifetime of the handle, because
+ *         fused calls read it on every call.
+ *  N, K   weight rows (output features) and columns (input features).
+ *         Requires N >= 1, K >= 8, K % 8 == 0, N*K % QK == 0.
+ *  flags  MQ_REG_* bits.
+ *  stream decode kernels are enqueued here; the cache is ready when this
+ *         stream's work up to this call has completed.
+ *  out    receives the handle.
+ *
+ * Cache layout: f16 [N, ldk] row-major, ldk = K + 64 if (2K) % 2048 == 0
+ * (K % 1024 == 0) else K; the pad columns hold +0.0.  The cache is
+ * library-owned and freed by mq_release_weight().
+ * Errors: MQ_ERR_UNSUPPORTED_TYPE, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_INVALID,
+ * MQ_ERR_OOM (nothing is left allocated), MQ_ERR_CUDA.
+ */
+int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K,
+                       uint32_t flags, void *stream, mq_handle *out);
+
+/* Free the handle and its f16 cache (synchronizes the device first so no
+ * enqueued call still reads it).  Never touches qdata.  Errors: MQ_ERR_INVALID. */
+int mq_release_weight(mq_handle w);
+
+/* Query a handle.  Any output pointer may be NULL.  *f16_cache is NULL for a
+ * MQ_REG_NO_CACHE handle.  Errors: MQ_ERR_INVALID. */
+int mq_weight_info(mq_handle w, int64_t *N, int64_t *K, int64_t *ldk,
+                   const void **f16_cache);
+
+/*
+ * mq_dequantize -- decode a flat block stream into f16 W[N,K] with row
+ * stride ldo (>= K, ldo % 8 == 0).  Columns [K, ldo) are left untouched.
+ * This is the decoder the cache is built with, exposed on its own.
+ * Passage: "05 · 8p", section 3.2, second site (the dequant kernel; 2-byte
+ * aligned blocks are read without wider misaligned loads).
+ * qdata and out_f16 are device pointers, 16-byte aligned.
+ * Errors: MQ_ERR_UNSUPPORTED_TYPE, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_INVALID,
+ * MQ_ERR_CUDA.
+ */
+int mq_dequantize(mq_type type, const void *qdata, int64_t N, int64_t K,
+                  void *out_f16, int64_t ldo, void *stream);
+
+/*
+ * mq_gemm -- cached path: Y[M,N] = X[M,K] . Wc[:, :K]^T with the f16 cache,
+ * f16 x f16 products accumulated in f32 on the tensor cores ("05 · 8p",
+ * section 2, persistent f16 cache; "Eager GPU Offload Without A Compute
+ * Graph", section "Storage and transfer reuse": f16 inputs, f32 output; when
+ * the output grid underfills the GPU, K is split and the partial planes are
+ * reduced in a fixed order on the same stream).
+ *  x  device f16 [M,K], 16-byte aligned.   y  device f32 [M,N], 16-byte aligned.
+ *  M  number of tokens, M >= 1.
+ * Results are bitwise reproducible from call to call for the same M.
+ * Errors: MQ_ERR_INVALID, MQ_ERR_NO_CACHE, MQ_ERR_SHAPE, MQ_ERR_ALIGN,
+ * MQ_ERR_OOM (split-K workspace), MQ_ERR_CUDA.
+ */
+int mq_gemm(const void *x, mq_handle w, float *y, int64_t M, void *stream);
+
+/*
+ * mq_gemm_fused -- fused path: same Y, decoding the raw blocks of qdata on
+ * chip into the f16 MMA operand ("05 · 8p", section 2: B tiles staged as
+ * quantized bytes and dequantized before the MMA; zero extra VRAM).  The
+ * on-chip decode produces the same f16 values as the cache.
+ * Extra preconditions: K % 64 == 0 (a 64-element K chunk never straddles a
+ * block), and the stream length (N*K/QK blocks times the block bytes) is a
+ * multiple of 16 bytes.  Errors as mq_gemm, minus MQ_ERR_NO_CACHE.
+ */
+int mq_gemm_fused(const void *x, mq_handle w, float *y, int64_t M, void *stream);
+
+/*
+ * mq_gemm_auto -- M gate: fused when M < gate (and the handle allows it),
+ * cached otherwise ("ggml-cuda: GEMM weight row padding ...", Summary: the
+ * f16 path is a large-batch win; the threshold is a token count per call).
+ * The gate is mq_get_m_gate(); environment variable MQ_M_GATE overrides it.
+ */
+int mq_gemm_auto(const void *x, mq_handle w, float *y, int64_t M, void *stream);
+
+/* Current M gate and a setter (value >= 1). */
+int64_t mq_get_m_gate(void);
+int mq_set_m_gate(int64_t m);
+
+/*
+ * mq_reserve_workspace -- grow the library's split-K workspace to at least
+ * `bytes` on the current device (never shrinks).  Call it before capturing
+ * mq_gemm* into a CUDA graph: inside a capture the library never allocates
+ * and, if the workspace is too small, it runs without split-K instead.
+ * The workspace serves one stream at a time: calls on different streams
+ * that overlap on the device must not share it.  Errors: MQ_ERR_OOM.
+ */
+int mq_reserve_workspace(int64_t bytes);
+
+/*
+ * mq_stream_status -- synchronize `stream`, then read and clear the
+ * library's device status word.  MQ_ERR_DEVICE if a kernel gave up on a
+ * bounded wait (every pipeline wait in the library's kernels has a time
+ * limit, after which the kernel records the error and exits cleanly instead
+ * of hanging); MQ_ERR_CUDA if the CUDA context reports an error (sticky
+ * errors are reported, not cleared: "Eager GPU Offload Without A Compute
+ * Graph", section "Ordering and unavoidable synchronization" -- a deferred
+ * device error found at the host boundary is fatal).
+ */
+int mq_stream_status(void *stream);
+
+/* Number of kernel launches the library has made since load (all kinds). */
+int64_t mq_launch_count(void);
+
+/* Static description of a status code. */
+const char *mq_error_string(int status);
+
+/* Detail of the last failure on the calling thread (argument and reason). */
+const char *mq_last_error_detail(void);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int mq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQ_H */

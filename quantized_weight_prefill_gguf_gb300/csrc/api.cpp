@@ -1,0 +1,551 @@
+// api.cpp -- the C ABI declared in include/mq.h: argument validation,
+// handles, the f16 cache, the split-K workspace, the device status word,
+// tensor-map encoding, the M gate and dispatch to the kernels.
+//
+// Nothing here computes on the host: every step of the GEMM and of the
+// decode runs in the library's CUDA kernels.  There is no CPU fallback; a
+// missing device or kernel image is an error.
+#include "mq.h"
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_set>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "mq_internal.h"
+
+struct mq_weight {
+    int type;
+    int64_t N, K, ldk;
+    int64_t nblocks;
+    int qk, bb;
+    const uint8_t *qdata;
+    __half *cache;       // null when registered with MQ_REG_NO_CACHE
+    int device;
+    CUtensorMap tm_cache;
+};
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+std::unordered_set<mq_weight *> g_live;
+thread_local std::string t_detail;
+std::atomic<int64_t> g_launches{0};
+std::atomic<int64_t> g_gate{-1};
+
+struct DevState {
+    bool init = false;
+    int sms = 0;
+    unsigned *status = nullptr;
+    float *ws = nullptr;
+    int64_t ws_bytes = 0;
+};
+DevState g_dev[kMaxDevices];
+
+int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_detail = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(MQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool log_on()
+{
+    static int on = -1;
+    if (on < 0) {
+        const char *v = getenv("MQ_LOG");
+        on = (v && *v && *v != '0') ? 1 : 0;
+    }
+    return on == 1;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool block_format(int type, int &qk, int &bb)
+{
+    switch (type) {
+    case MQ_TYPE_Q8_0: qk = 32; bb = 34; return true;
+    case MQ_TYPE_Q4_K: qk = 256; bb = 144; return true;
+    case MQ_TYPE_Q6_K: qk = 256; bb = 210; return true;
+    default: return false;
+    }
+}
+
+// Current device's state, created on first use: SM count, status word.
+int device_state(DevState **out, int *dev_out = nullptr)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(MQ_ERR_NO_DEVICE, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(MQ_ERR_NO_DEVICE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState &d = g_dev[dev];
+    if (!d.init) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetDeviceProperties");
+        if (prop.major != 10 || prop.minor != 3)
+            return fail(MQ_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                        prop.major, prop.minor);
+        e = cudaMalloc(&d.status, sizeof(unsigned));
+        if (e != cudaSuccess)
+            return fail(MQ_ERR_OOM, "status word: %s", cudaGetErrorString(e));
+        e = cudaMemset(d.status, 0, sizeof(unsigned));
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(status)");
+        d.sms = prop.multiProcessorCount;
+        d.init = true;
+    }
+    *out = &d;
+    if (dev_out)
+        *dev_out = dev;
+    return MQ_OK;
+}
+
+// Grow the workspace of `d` to `bytes` (synchronizes the device before
+// freeing the old buffer, so no enqueued kernel still uses it).
+int grow_workspace(DevState &d, int64_t bytes)
+{
+    if (bytes <= d.ws_bytes)
+        return MQ_OK;
+    if (d.ws) {
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceSynchronize before workspace growth");
+        cudaFree(d.ws);
+        d.ws = nullptr;
+        d.ws_bytes = 0;
+    }
+    void *p = nullptr;
+    cudaError_t e = cudaMalloc(&p, static_cast<size_t>(bytes));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(MQ_ERR_OOM, "split-K workspace of %lld bytes: %s", (long long)bytes, cudaGetErrorString(e));
+    }
+    d.ws = static_cast<float *>(p);
+    d.ws_bytes = bytes;
+    return MQ_OK;
+}
+
+int check_handle(mq_handle w)
+{
+    if (!w)
+        return fail(MQ_ERR_INVALID, "handle is NULL");
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_live.count(w))
+        return fail(MQ_ERR_INVALID, "handle %p is not a live registered weight (released or never registered)",
+                    (void *)w);
+    return MQ_OK;
+}
+
+int64_t env_int(const char *name, int64_t dflt)
+{
+    const char *v = getenv(name);
+    if (!v || !*v)
+        return dflt;
+    char *end = nullptr;
+    long long x = strtoll(v, &end, 10);
+    return (end && *end == '\0') ? x : dflt;
+}
+
+// Token count at and above which mq_gemm_auto takes the cached path.
+int64_t current_gate()
+{
+    int64_t g = g_gate.load();
+    if (g > 0)
+        return g;
+    return env_int("MQ_M_GATE", 64);
+}
+
+// Plan, workspace and launch of one GEMM (cached or fused).
+int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bool fused)
+{
+    DevState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc)
+        return rc;
+
+    const bool splitk_on = env_int("MQ_SPLITK", 1) != 0;
+    const int64_t want = splitk_on ? mq::plan_ws_bytes_wanted(M, w->N, w->K, d->sms) : 0;
+    if (want > d->ws_bytes) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(s, &cs);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaStreamIsCapturing");
+        if (cs == cudaStreamCaptureStatusNone) {
+            std::lock_guard<std::mutex> lk(g_mu);
+            rc = grow_workspace(*d, want);
+            if (rc)
+                return rc;
+        }
+    }
+    const mq::GemmPlan plan = mq::plan_gemm(M, w->N, w->K, d->sms, fused, splitk_on ? d->ws_bytes : 0);
+
+    CUtensorMap tm_x;
+    CUresult cr = mq::encode_f16_2d(&tm_x, x, M, w->K, w->K, 64, plan.bn);
+    if (cr != CUDA_SUCCESS)
+        return fail(MQ_ERR_CUDA, "tensor map for x (M=%lld, K=%lld, box 64x%d): CUresult %d", (long long)M,
+                    (long long)w->K, plan.bn, (int)cr);
+
+    mq::GemmArgs a{};
+    a.y = y;
+    a.ws = d->ws;
+    a.status = d->status;
+    a.wq = w->qdata;
+    a.M = M;
+    a.N = w->N;
+    a.K = w->K;
+    a.m_tiles = static_cast<int>((M + plan.bn - 1) / plan.bn);
+    a.n_tiles = static_cast<int>((w->N + 127) / 128);
+    a.kblocks = static_cast<int>((w->K + 63) / 64);
+    a.full_tiles = plan.full_tiles;
+    a.split = plan.split;
+    a.units = plan.units;
+    a.qtype = w->type;
+
+    if (log_on())
+        fprintf(stderr, "[mq] %s M=%lld N=%lld K=%lld bn=%d tiles=%d split=%d full=%d units=%d grid=%d\n",
+                fused ? "fused" : "cached", (long long)M, (long long)w->N, (long long)w->K, plan.bn, plan.tiles,
+                plan.split, plan.full_tiles, plan.units, plan.grid);
+
+    cudaError_t e = fused ? mq::launch_gemm_fused(tm_x, a, plan, s) : mq::launch_gemm_cached(w->tm_cache, tm_x, a, plan, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, fused ? "fused GEMM launch" : "cached GEMM launch");
+    e = mq::launch_splitk_reduce(a, plan, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "split-K reduce launch");
+    return MQ_OK;
+}
+
+int check_gemm_args(const void *x, mq_handle w, float *y, int64_t M)
+{
+    int rc = check_handle(w);
+    if (rc)
+        return rc;
+    if (!x)
+        return fail(MQ_ERR_INVALID, "x is NULL");
+    if (!y)
+        return fail(MQ_ERR_INVALID, "y is NULL");
+    if (M < 1)
+        return fail(MQ_ERR_SHAPE, "M=%lld: need M >= 1", (long long)M);
+    if (M > 0x7FFFFFFFLL)
+        return fail(MQ_ERR_SHAPE, "M=%lld exceeds 2^31-1", (long long)M);
+    if (!aligned16(x))
+        return fail(MQ_ERR_ALIGN, "x=%p is not 16-byte aligned", x);
+    if (!aligned16(y))
+        return fail(MQ_ERR_ALIGN, "y=%p is not 16-byte aligned", (void *)y);
+    return MQ_OK;
+}
+
+}  // namespace
+
+namespace mq {
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+CUresult encode_f16_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                       int box_rows)
+{
+    static PFN_encodeTiled fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p)
+            return CUDA_ERROR_NOT_FOUND;
+        fn = reinterpret_cast<PFN_encodeTiled>(p);
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace mq
+
+extern "C" {
+
+int mq_version(void) { return 100; }
+
+int64_t mq_launch_count(void) { return g_launches.load(); }
+
+const char *mq_last_error_detail(void) { return t_detail.c_str(); }
+
+const char *mq_error_string(int status)
+{
+    switch (status) {
+    case MQ_OK: return "ok";
+    case MQ_ERR_INVALID: return "invalid argument or handle";
+    case MQ_ERR_UNSUPPORTED_TYPE: return "unsupported block type";
+    case MQ_ERR_SHAPE: return "shape precondition violated";
+    case MQ_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case MQ_ERR_NO_CACHE: return "weight has no f16 cache";
+    case MQ_ERR_OOM: return "device allocation failed";
+    case MQ_ERR_CUDA: return "CUDA error";
+    case MQ_ERR_DEVICE: return "device-side error flagged by a kernel";
+    case MQ_ERR_NO_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status";
+    }
+}
+
+int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, uint32_t flags, void *stream,
+                       mq_handle *out)
+{
+    if (!out)
+        return fail(MQ_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    int qk = 0, bb = 0;
+    if (!block_format(type, qk, bb))
+        return fail(MQ_ERR_UNSUPPORTED_TYPE,
+                    "type id %d is not supported (supported: Q8_0=8, Q4_K=12, Q6_K=14); the weight has no kernel",
+                    (int)type);
+    if (flags & ~(MQ_REG_NO_CACHE | MQ_REG_NO_KPAD | MQ_REG_KPAD))
+        return fail(MQ_ERR_INVALID, "unknown flag bits 0x%x", flags);
+    if ((flags & MQ_REG_NO_KPAD) && (flags & MQ_REG_KPAD))
+        return fail(MQ_ERR_INVALID, "MQ_REG_NO_KPAD and MQ_REG_KPAD are exclusive");
+    if (!qdata)
+        return fail(MQ_ERR_INVALID, "qdata is NULL");
+    if (N < 1 || K < 8 || (K % 8) != 0)
+        return fail(MQ_ERR_SHAPE, "N=%lld K=%lld: need N >= 1, K >= 8, K %% 8 == 0", (long long)N, (long long)K);
+    if (N > 0x7FFFFFFFLL || K > 0x7FFFFFFFLL)
+        return fail(MQ_ERR_SHAPE, "N=%lld K=%lld: each must be below 2^31", (long long)N, (long long)K);
+    if ((N * K) % qk != 0)
+        return fail(MQ_ERR_SHAPE, "N*K=%lld is not a whole number of %d-element blocks", (long long)(N * K), qk);
+    if (!aligned16(qdata))
+        return fail(MQ_ERR_ALIGN, "qdata=%p is not 16-byte aligned", qdata);
+
+    DevState *d = nullptr;
+    int dev = 0;
+    int rc = device_state(&d, &dev);
+    if (rc)
+        return rc;
+
+    int64_t ldk = K;
+    const int64_t kpad_env = env_int("MQ_KPAD", -1);   // 0: never, 1: always, else by rule
+    if (flags & MQ_REG_KPAD)
+        ldk = K + 64;
+    else if (flags & MQ_REG_NO_KPAD)
+        ldk = K;
+    else if (kpad_env == 0)
+        ldk = K;
+    else if (kpad_env == 1)
+        ldk = K + 64;
+    else
+        ldk = ((2 * K) % 2048 == 0) ? K + 64 : K;
+
+    mq_weight *w = new mq_weight();
+    w->type = type;
+    w->N = N;
+    w->K = K;
+    w->ldk = ldk;
+    w->qk = qk;
+    w->bb = bb;
+    w->nblocks = N * K / qk;
+    w->qdata = static_cast<const uint8_t *>(qdata);
+    w->cache = nullptr;
+    w->device = dev;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!(flags & MQ_REG_NO_CACHE)) {
+        const size_t bytes = static_cast<size_t>(N) * static_cast<size_t>(ldk) * 2;
+        void *p = nullptr;
+        cudaError_t e = env_int("MQ_FAULT_ALLOC", 0) ? cudaErrorMemoryAllocation : cudaMalloc(&p, bytes);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            delete w;
+            return fail(MQ_ERR_OOM, "f16 cache of %zu bytes (N=%lld, ldk=%lld): %s", bytes, (long long)N,
+                        (long long)ldk, cudaGetErrorString(e));
+        }
+        w->cache = static_cast<__half *>(p);
+        e = mq::launch_dequant(type, qdata, w->nblocks, w->cache, K, ldk, s);
+        if (e == cudaSuccess && ldk > K)
+            e = cudaMemset2DAsync(w->cache + K, static_cast<size_t>(ldk) * 2, 0, static_cast<size_t>(ldk - K) * 2,
+                                  static_cast<size_t>(N), s);
+        if (e != cudaSuccess) {
+            cudaFree(w->cache);
+            delete w;
+            return cuda_fail(e, "decode into the f16 cache");
+        }
+        CUresult cr = mq::encode_f16_2d(&w->tm_cache, w->cache, N, K, ldk, 64, 128);
+        if (cr != CUDA_SUCCESS) {
+            cudaStreamSynchronize(s);
+            cudaFree(w->cache);
+            delete w;
+            return fail(MQ_ERR_CUDA, "tensor map for the f16 cache: CUresult %d", (int)cr);
+        }
+    }
+    if (log_on())
+        fprintf(stderr, "[mq] register type=%d N=%lld K=%lld ldk=%lld cache=%s\n", (int)type, (long long)N,
+                (long long)K, (long long)ldk, w->cache ? "yes" : "no");
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_live.insert(w);
+    }
+    *out = w;
+    return MQ_OK;
+}
+
+int mq_release_weight(mq_handle w)
+{
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!w || !g_live.count(w))
+            return fail(MQ_ERR_INVALID, "handle %p is not a live registered weight", (void *)w);
+        g_live.erase(w);
+    }
+    if (w->cache) {
+        int cur = 0;
+        cudaGetDevice(&cur);
+        cudaSetDevice(w->device);
+        cudaDeviceSynchronize();
+        cudaFree(w->cache);
+        cudaSetDevice(cur);
+    }
+    delete w;
+    return MQ_OK;
+}
+
+int mq_weight_info(mq_handle w, int64_t *N, int64_t *K, int64_t *ldk, const void **f16_cache)
+{
+    int rc = check_handle(w);
+    if (rc)
+        return rc;
+    if (N) *N = w->N;
+    if (K) *K = w->K;
+    if (ldk) *ldk = w->ldk;
+    if (f16_cache) *f16_cache = w->cache;
+    return MQ_OK;
+}
+
+int mq_dequantize(mq_type type, const void *qdata, int64_t N, int64_t K, void *out_f16, int64_t ldo, void *stream)
+{
+    int qk = 0, bb = 0;
+    if (!block_format(type, qk, bb))
+        return fail(MQ_ERR_UNSUPPORTED_TYPE, "type id %d is not supported (Q8_0=8, Q4_K=12, Q6_K=14)", (int)type);
+    if (!qdata || !out_f16)
+        return fail(MQ_ERR_INVALID, "%s is NULL", qdata ? "out_f16" : "qdata");
+    if (N < 1 || K < 8 || (K % 8) != 0 || ldo < K || (ldo % 8) != 0)
+        return fail(MQ_ERR_SHAPE, "N=%lld K=%lld ldo=%lld: need N >= 1, K >= 8, K %% 8 == 0, ldo >= K, ldo %% 8 == 0",
+                    (long long)N, (long long)K, (long long)ldo);
+    if ((N * K) % qk != 0)
+        return fail(MQ_ERR_SHAPE, "N*K=%lld is not a whole number of %d-element blocks", (long long)(N * K), qk);
+    if (!aligned16(qdata) || !aligned16(out_f16))
+        return fail(MQ_ERR_ALIGN, "%s is not 16-byte aligned", aligned16(qdata) ? "out_f16" : "qdata");
+    DevState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc)
+        return rc;
+    cudaError_t e = mq::launch_dequant(type, qdata, N * K / qk, static_cast<__half *>(out_f16), K, ldo,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "dequantize launch");
+    return MQ_OK;
+}
+
+int mq_gemm(const void *x, mq_handle w, float *y, int64_t M, void *stream)
+{
+    int rc = check_gemm_args(x, w, y, M);
+    if (rc)
+        return rc;
+    if (!w->cache)
+        return fail(MQ_ERR_NO_CACHE, "weight was registered with MQ_REG_NO_CACHE; use mq_gemm_fused");
+    return run_gemm(x, w, y, M, static_cast<cudaStream_t>(stream), false);
+}
+
+int mq_gemm_fused(const void *x, mq_handle w, float *y, int64_t M, void *stream)
+{
+    int rc = check_gemm_args(x, w, y, M);
+    if (rc)
+        return rc;
+    if (w->K % 64 != 0)
+        return fail(MQ_ERR_SHAPE, "fused path needs K %% 64 == 0 (K=%lld)", (long long)w->K);
+    if ((w->nblocks * w->bb) % 16 != 0)
+        return fail(MQ_ERR_SHAPE, "fused path needs the block stream length (%lld bytes) to be a multiple of 16",
+                    (long long)(w->nblocks * w->bb));
+    return run_gemm(x, w, y, M, static_cast<cudaStream_t>(stream), true);
+}
+
+int mq_gemm_auto(const void *x, mq_handle w, float *y, int64_t M, void *stream)
+{
+    int rc = check_gemm_args(x, w, y, M);
+    if (rc)
+        return rc;
+    const bool fused_ok = (w->K % 64 == 0) && ((w->nblocks * w->bb) % 16 == 0);
+    if (!w->cache || (M < current_gate() && fused_ok))
+        return mq_gemm_fused(x, w, y, M, stream);
+    return mq_gemm(x, w, y, M, stream);
+}
+
+int64_t mq_get_m_gate(void) { return current_gate(); }
+
+int mq_set_m_gate(int64_t m)
+{
+    if (m < 1)
+        return fail(MQ_ERR_INVALID, "gate %lld: need >= 1", (long long)m);
+    g_gate.store(m);
+    return MQ_OK;
+}
+
+int mq_reserve_workspace(int64_t bytes)
+{
+    if (bytes < 0)
+        return fail(MQ_ERR_INVALID, "bytes=%lld < 0", (long long)bytes);
+    DevState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc)
+        return rc;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return grow_workspace(*d, bytes);
+}
+
+int mq_stream_status(void *stream)
+{
+    DevState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc)
+        return rc;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned st = 0;
+    e = cudaMemcpy(&st, d->status, sizeof st, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the device status word");
+    if (st != 0) {
+        cudaMemset(d->status, 0, sizeof st);
+        return fail(MQ_ERR_DEVICE, "device status 0x%x:%s%s", st, (st & 1u) ? " pipeline wait timed out" : "",
+                    (st & 2u) ? " kernel rejected its arguments" : "");
+    }
+    return MQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// mq_internal.h -- host-side interface between the C ABI (api.cpp) and the
+// kernel translation units.  Not installed; no torch types anywhere.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace mq {
+
+// Counts every kernel launch the library makes (reported by mq_launch_count).
+void note_launch();
+
+// ---------------------------------------------------------------- decoders
+cudaError_t launch_dequant(int type, const void *q, int64_t nblocks, __half *out, int64_t K, int64_t ldo,
+                           cudaStream_t s);
+
+// ---------------------------------------------------------------- GEMMs
+// Work decomposition of one GEMM: the output is cut into tiles of 128
+// weight rows (MMA M) x BN tokens (MMA N); tiles [0, full_tiles) run over
+// all of K in one unit, the remaining tiles are split into `split` K-ranges
+// whose f32 partial planes go to the workspace and are summed in fixed
+// order p = 0..split-1 by the reduce kernel.
+struct GemmArgs {
+    float *y;            // [M, N] f32 output
+    float *ws;           // split-K partial planes: [slot][part][BN][128]
+    unsigned *status;    // device status word
+    const uint8_t *wq;   // raw quantized stream (fused path)
+    int64_t M, N, K;
+    int m_tiles, n_tiles;
+    int kblocks;         // ceil(K / 64)
+    int full_tiles;
+    int split;
+    int units;
+    int qtype;           // fused path: GGUF type id
+};
+
+struct GemmPlan {
+    int bn;              // tokens per tile (MMA N)
+    int split;
+    int full_tiles;
+    int tiles;
+    int units;
+    int grid;
+    int64_t ws_bytes;
+};
+
+// Choose tile width, split-K and grid for an M x N x K problem on `sms` SMs.
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available);
+
+// Workspace bytes the plan would use with an unlimited workspace.
+int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms);
+
+// Cached path: tm_w maps the f16 cache [N, ldk] (box 64 x 128), tm_x maps
+// X [M, K] (box 64 x bn).  Both 128-byte swizzled.
+cudaError_t launch_gemm_cached(const CUtensorMap &tm_w, const CUtensorMap &tm_x, const GemmArgs &a,
+                               const GemmPlan &p, cudaStream_t s);
+
+// Fused path: tm_x as above; the weight is read from a.wq.
+cudaError_t launch_gemm_fused(const CUtensorMap &tm_x, const GemmArgs &a, const GemmPlan &p, cudaStream_t s);
+
+// Fixed-order sum of the split-K partial planes into Y.
+cudaError_t launch_splitk_reduce(const GemmArgs &a, const GemmPlan &p, cudaStream_t s);
+
+// ---------------------------------------------------------------- tensor maps
+// Encode a 2-D f16 row-major [rows, cols] tensor map with row stride `ld`
+// elements, a box of box_cols x box_rows and 128-byte swizzle.
+CUresult encode_f16_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld,
+                       int box_cols, int box_rows);
+
+}  // namespace mq
