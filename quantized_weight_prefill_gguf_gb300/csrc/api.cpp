@@ -187,7 +187,7 @@ int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bo
         return rc;
 
     const bool splitk_on = env_int("MQ_SPLITK", 1) != 0;
-    const int64_t want = splitk_on ? mq::plan_ws_bytes_wanted(M, w->N, w->K, d->sms) : 0;
+    const int64_t want = splitk_on ? mq::plan_ws_bytes_wanted(M, w->N, w->K, d->sms, fused) : 0;
     if (want > d->ws_bytes) {
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         cudaError_t e = cudaStreamIsCapturing(s, &cs);
@@ -222,6 +222,7 @@ int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bo
     a.full_tiles = plan.full_tiles;
     a.split = plan.split;
     a.units = plan.units;
+    a.kb_align = plan.kb_align;
     a.qtype = w->type;
 
     if (log_on())

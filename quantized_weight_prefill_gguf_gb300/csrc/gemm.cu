@@ -33,14 +33,12 @@
 
 #include "mq_internal.h"
 #include "mq_ptx.cuh"
+#include "mq_tile.cuh"
 
 namespace mq {
 
 namespace {
 
-constexpr int kBK = 64;                       // K elements per stage (one 128-byte swizzle row)
-constexpr int kTileRows = 128;                // weight rows per tile (MMA M)
-constexpr int kABytes = kTileRows * kBK * 2;  // 16 KB
 constexpr int kThreads = 192;
 
 template <int BN> struct Cfg {
@@ -49,30 +47,6 @@ template <int BN> struct Cfg {
     static constexpr int kTmemCols = 2 * BN;   // two accumulators
     static constexpr int kSmem = 1024 + kStages * (kABytes + kBBytes) + 256;
 };
-
-struct UnitInfo {
-    int tile, kb0, kb1, part, slot;
-};
-
-__device__ __forceinline__ UnitInfo unit_info(const GemmArgs &a, int u)
-{
-    UnitInfo r;
-    if (u < a.full_tiles) {
-        r.tile = u;
-        r.kb0 = 0;
-        r.kb1 = a.kblocks;
-        r.part = -1;
-        r.slot = 0;
-    } else {
-        const int v = u - a.full_tiles;
-        r.slot = v / a.split;
-        r.part = v - r.slot * a.split;
-        r.tile = a.full_tiles + r.slot;
-        r.kb0 = static_cast<int>(static_cast<int64_t>(r.part) * a.kblocks / a.split);
-        r.kb1 = static_cast<int>(static_cast<int64_t>(r.part + 1) * a.kblocks / a.split);
-    }
-    return r;
-}
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -205,50 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue: warps 2..5 own TMEM lane quarters 2,3,0,1
-        const int q = warp & 3;
-        const int row = q * 32 + lane;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-            const UnitInfo ui = unit_info(a, u);
-            const bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, a.status);
-            if (!__all_sync(0xFFFFFFFFu, ok))
-                break;
-            tc_fence_after();
-            const int64_t n = static_cast<int64_t>(ui.tile / a.m_tiles) * kTileRows + row;
-            const int64_t m0 = static_cast<int64_t>(ui.tile % a.m_tiles) * BN;
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + c),
-                                   r);
-                tmem_ld_wait();
-                if (ui.part < 0) {
-                    if (n < a.N) {
-                        float *yp = a.y + (m0 + c) * a.N + n;
-                        const int64_t rem = a.M - (m0 + c);
-                        const int lim = rem < 32 ? static_cast<int>(rem) : 32;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < lim)
-                                yp[static_cast<int64_t>(j) * a.N] = __uint_as_float(r[j]);
-                    }
-                } else {
-                    float *wp = a.ws + ((static_cast<int64_t>(ui.slot) * a.split + ui.part) * BN + c) * kTileRows + row;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        wp[j * kTileRows] = __uint_as_float(r[j]);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&tempty[acc]);
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1u;
-            }
-        }
+        epilogue_role<BN>(a, tmem, tfull, tempty, abort_flag, warp, lane);
     }
 
     tc_fence_before();
@@ -260,24 +191,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Fixed-order split-K reduction: Y = sum over p = 0..split-1 of the partial
-// planes, p ascending, for the split tiles.  One CTA per split tile.
+// planes, p ascending, for the split tiles.  Grid (bn/8, slots): each thread
+// owns 4 consecutive weight rows of one token column, loads all split
+// partials first (so their latencies overlap) and adds them in order.
+constexpr int kMaxSplit = 8;
+
 __global__ void __launch_bounds__(256) k_splitk_reduce(const GemmArgs a, int bn)
 {
-    const int slot = blockIdx.x;
+    const int slot = blockIdx.y;
     const int tile = a.full_tiles + slot;
-    const int64_t n0 = static_cast<int64_t>(tile / a.m_tiles) * kTileRows;
-    const int64_t m0 = static_cast<int64_t>(tile % a.m_tiles) * bn;
     const int64_t plane = static_cast<int64_t>(bn) * kTileRows;
-    const float *base = a.ws + static_cast<int64_t>(slot) * a.split * plane;
-    for (int e = threadIdx.x; e < bn * kTileRows; e += blockDim.x) {
-        const int col = e >> 7, row = e & 127;
-        const int64_t m = m0 + col, n = n0 + row;
-        if (m < a.M && n < a.N) {
-            float acc = base[e];
-            for (int p = 1; p < a.split; ++p)
-                acc = __fadd_rn(acc, base[p * plane + e]);
-            a.y[m * a.N + n] = acc;
+    const int e = (blockIdx.x * 256 + threadIdx.x) * 4;
+    if (e >= plane)
+        return;
+    const int col = e >> 7, row = e & 127;
+    const int64_t m = static_cast<int64_t>(tile % a.m_tiles) * bn + col;
+    const int64_t n = static_cast<int64_t>(tile / a.m_tiles) * kTileRows + row;
+    if (m >= a.M || n >= a.N)
+        return;
+    const float4 *base = reinterpret_cast<const float4 *>(a.ws + static_cast<int64_t>(slot) * a.split * plane + e);
+    float4 v[kMaxSplit];
+#pragma unroll
+    for (int p = 0; p < kMaxSplit; ++p)
+        if (p < a.split)
+            v[p] = __ldcs(base + p * (plane / 4));
+    float4 acc = v[0];
+#pragma unroll
+    for (int p = 1; p < kMaxSplit; ++p)
+        if (p < a.split) {
+            acc.x = __fadd_rn(acc.x, v[p].x);
+            acc.y = __fadd_rn(acc.y, v[p].y);
+            acc.z = __fadd_rn(acc.z, v[p].z);
+            acc.w = __fadd_rn(acc.w, v[p].w);
         }
+    float *yp = a.y + m * a.N + n;
+    if ((a.N & 3) == 0 && n + 3 < a.N) {
+        *reinterpret_cast<float4 *>(yp) = acc;
+    } else {
+        const float r[4] = {acc.x, acc.y, acc.z, acc.w};
+        for (int i = 0; i < 4 && n + i < a.N; ++i)
+            yp[i] = r[i];
     }
 }
 
@@ -307,12 +260,15 @@ cudaError_t launch_bn(const CUtensorMap &tw, const CUtensorMap &tx, const GemmAr
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available)
 {
-    (void)fused;
     GemmPlan p{};
     p.bn = M > 128 ? 256 : (M > 64 ? 128 : (M > 32 ? 64 : 32));
+    // The fused path stages raw weight bytes 256 K-elements (4 K steps) at a
+    // time, so its split boundaries fall on multiples of 4 K steps.
+    p.kb_align = fused ? 4 : 1;
     const int64_t m_tiles = (M + p.bn - 1) / p.bn;
     const int64_t n_tiles = (N + kTileRows - 1) / kTileRows;
     const int64_t kblocks = (K + kBK - 1) / kBK;
+    const int64_t groups = (kblocks + p.kb_align - 1) / p.kb_align;
     p.tiles = static_cast<int>(m_tiles * n_tiles);
     p.split = 1;
     p.full_tiles = p.tiles;
@@ -321,8 +277,9 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t
     const int tail = p.tiles % sms;
     if (tail != 0) {
         int s = sms / tail;
-        s = static_cast<int>(std::min<int64_t>(s, std::max<int64_t>(1, kblocks / 4)));
-        s = std::min(s, 8);
+        const int64_t max_parts = fused ? groups : std::max<int64_t>(1, kblocks / 4);
+        s = static_cast<int>(std::min<int64_t>(s, max_parts));
+        s = std::min(s, kMaxSplit);
         if (s >= 2) {
             const int64_t bytes = static_cast<int64_t>(tail) * s * p.bn * kTileRows * 4;
             if (bytes <= ws_available) {
@@ -337,9 +294,9 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t
     return p;
 }
 
-int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms)
+int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused)
 {
-    return plan_gemm(M, N, K, sms, false, INT64_MAX).ws_bytes;
+    return plan_gemm(M, N, K, sms, fused, INT64_MAX).ws_bytes;
 }
 
 cudaError_t launch_gemm_cached(const CUtensorMap &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p,
@@ -359,7 +316,9 @@ cudaError_t launch_splitk_reduce(const GemmArgs &a, const GemmPlan &p, cudaStrea
     const int slots = p.tiles - p.full_tiles;
     if (slots <= 0 || p.split <= 1)
         return cudaSuccess;
-    k_splitk_reduce<<<slots, 256, 0, s>>>(a, p.bn);
+    if (p.split > kMaxSplit)
+        return cudaErrorInvalidValue;
+    k_splitk_reduce<<<dim3(p.bn / 8, slots), 256, 0, s>>>(a, p.bn);
     note_launch();
     return cudaGetLastError();
 }

@@ -33,11 +33,16 @@ struct GemmArgs {
     int full_tiles;
     int split;
     int units;
+    int kb_align;        // split boundaries are multiples of this many K steps
     int qtype;           // fused path: GGUF type id
+    int raw_rs;          // fused path: shared-memory bytes per weight row of a raw stage
+    int raw_stages;      // fused path: raw stages in the ring
+    int stages;          // fused path: f16 operand stages in the ring
 };
 
 struct GemmPlan {
     int bn;              // tokens per tile (MMA N)
+    int kb_align;        // split boundaries in K steps (4 for the fused path)
     int split;
     int full_tiles;
     int tiles;
@@ -50,7 +55,7 @@ struct GemmPlan {
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available);
 
 // Workspace bytes the plan would use with an unlimited workspace.
-int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms);
+int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused);
 
 // Cached path: tm_w maps the f16 cache [N, ldk] (box 64 x 128), tm_x maps
 // X [M, K] (box 64 x bn).  Both 128-byte swizzled.
