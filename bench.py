@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Prefill-GEMM benchmark of one Qwen2.5-7B-shaped layer on GB300.
+
+One step = the layer's seven prefill GEMMs Y = X . W^T at M = 2048 tokens
+through the library's public call mq_gemm_auto (the M gate sends M = 2048 to
+the cached path: tcgen05 GEMM on the f16 cache, split-K tail + fixed-order
+reduce where the tile grid underfills the GPU).  Weights q/k/v/o/gate/up are
+Q4_K, down is Q6_K, all seeded synthetic bytes with the model's shapes; they
+are registered (decoded once into the f16 cache) before timing.
+
+Printed: one JSON line (rank 0) with the contract keys plus
+  roofline      the cached GEMM kernel against the measured dense peak, its
+                per-launch duration read from CUDA events that the library
+                records on the launching stream during the timed steps;
+  cpu_baseline  the CPU oracle (f64) on a bounded sample of the same layer;
+  e2e           the same metric with host buffers: pinned-host inputs copied
+                in and all outputs copied out inside the timed region;
+  decode        the one-time decoders (registration) against HBM bandwidth;
+  small_m       fused vs cached over the small-M sweep (crossover, HBM GB/s).
+
+--impl reference times the CPU oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from quantized_weight_prefill_gguf_gb300 import synth  # noqa: E402
+
+METRIC = "prefill GEMM TFLOP/s & tok/s per 7B layer at M=2048; % of f16 TC / HBM roofline"
+WORKLOAD = "qwen2.5-7b_layer"
+M_TOKENS = 2048
+L2_BYTES = 126 * 1024 * 1024
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def layer_flops(weights, M):
+    return sum(2.0 * M * w.N * w.K for w in weights)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, out_path: str | None = None):
+        self.gpu = gpu_index
+        self.out_path = out_path
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if self.out_path:
+            with open(self.out_path, "w") as fh:
+                fh.write("\n".join(self.lines) + "\n")
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- reference arm (CPU oracle)
+
+def oracle_cpu_run(weights, xs, budget_s: float, min_tokens: int = 1):
+    """Time the oracle's f64 GEMM over the layer on a token sample sized to
+    about budget_s seconds.  Returns (tflops, tokens, seconds, decode_s, threads)."""
+    import oracle
+    orc = oracle.load()
+    t0 = time.perf_counter()
+    W16 = [orc.decode_matrix(w.qtype, w.data, w.N, w.K) for w in weights]
+    decode_s = time.perf_counter() - t0
+    # calibrate on 4 tokens, then size the sample
+    t0 = time.perf_counter()
+    for w, W in zip(weights, W16):
+        orc.gemm_f64(xs[w.K][:4].view(np.uint16), W)
+    cal = time.perf_counter() - t0
+    per_token = cal / 4
+    tokens = int(max(min_tokens, min(M_TOKENS, budget_s / max(per_token, 1e-9))))
+    t0 = time.perf_counter()
+    for w, W in zip(weights, W16):
+        orc.gemm_f64(xs[w.K][:tokens].view(np.uint16), W)
+    secs = time.perf_counter() - t0
+    tflops = layer_flops(weights, tokens) / secs / 1e12
+    return tflops, tokens, secs, decode_s, orc.num_threads()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    weights, xs = synth.workload(WORKLOAD, seed=0)
+    import oracle
+    orc = oracle.load()
+    W16 = [orc.decode_matrix(w.qtype, w.data, w.N, w.K) for w in weights]
+    # size each step so the whole run takes about two minutes
+    t0 = time.perf_counter()
+    for w, W in zip(weights, W16):
+        orc.gemm_f64(xs[w.K][:2].view(np.uint16), W)
+    per_token = (time.perf_counter() - t0) / 2
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    tokens = int(max(1, min(M_TOKENS, budget / per_token)))
+
+    def step():
+        for w, W in zip(weights, W16):
+            orc.gemm_f64(xs[w.K][:tokens].view(np.uint16), W)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = time.perf_counter() - t0
+    flops = layer_flops(weights, tokens) * args.steps
+    value = flops / secs / 1e12
+    sample = (f"{tokens} of the {M_TOKENS} tokens per step through all 7 GEMMs of the layer "
+              f"(f64 accumulation, weights decoded once by the oracle before timing)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_TOKENS, "tokens_per_step_sampled": tokens},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget for cpu_baseline")
+    ap.add_argument("--no-extras", action="store_true", help="skip e2e, small-M sweep and cpu_baseline")
+    ap.add_argument("--clocks-out", default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import quantized_weight_prefill_gguf_gb300 as mq
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    P = peaks()
+    weights, xs = synth.workload(WORKLOAD, seed=0)
+    # each rank processes its own batch of tokens (independent prefill u-batches)
+    if rank > 0:
+        g = synth.rng(1000 + rank)
+        xs = {k: synth.activations(g, M_TOKENS, k) for k in xs}
+
+    stream = torch.cuda.current_stream()
+    qdev = [torch.from_numpy(w.data).cuda() for w in weights]
+    torch.cuda.synchronize()
+
+    # registration = one-time decode into the f16 caches, traced per weight
+    mq.mq_trace_enable(True)
+    handles = [mq.mq_register_weight(w.qtype, q, w.N, w.K) for w, q in zip(weights, qdev)]
+    torch.cuda.synchronize()
+    dec = [r for r in mq.mq_trace_records() if r["kind"] == mq.MQ_TRACE_DECODE]
+    mq.mq_trace_enable(False)
+    decode_bytes = sum(synth.nblocks(w.qtype, w.N, w.K) * synth.BLOCK[w.qtype][1] + 2 * w.N * w.K for w in weights)
+    decode_ms = sum(r["ms_main"] for r in dec)
+
+    xdev = {k: torch.from_numpy(v).cuda() for k, v in xs.items()}
+    ys = [torch.empty((M_TOKENS, w.N), dtype=torch.float32, device="cuda") for w in weights]
+    mq.mq_reserve_workspace(64 << 20)
+
+    def step(xmap):
+        for w, h, y in zip(weights, handles, ys):
+            mq.mq_gemm_auto(xmap[w.K], h, y, M_TOKENS, stream)
+
+    for _ in range(args.warmup):
+        step(xdev)
+    torch.cuda.synchronize()
+    mq.mq_stream_status()
+
+    # ---- timed region
+    clocks = ClockSampler(local_rank, args.clocks_out)
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = mq.mq_launch_count()
+    mq.mq_trace_enable(True)
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(xdev)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    mq.mq_trace_enable(False)
+    launches = mq.mq_launch_count() - launches0
+    clk = clocks.stop()
+    mq.mq_stream_status()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    flops_step = layer_flops(weights, M_TOKENS)
+    value = world * flops_step / (ms * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel: the cached GEMM (k_gemm_cached)
+    recs = mq.mq_trace_records()
+    gem = [r for r in recs if r["kind"] == mq.MQ_TRACE_GEMM_CACHED]
+    g_flops = sum(2.0 * r["M"] * r["N"] * r["K"] for r in gem)
+    g_ms = sum(r["ms_main"] for r in gem)
+    red_ms = sum(r["ms_aux"] for r in gem)
+    per_gemm = []
+    for w in weights:
+        rs = [r for r in gem if r["N"] == w.N and r["K"] == w.K]
+        if rs:
+            t_main = statistics.median(r["ms_main"] for r in rs)
+            t_aux = statistics.median(r["ms_aux"] for r in rs)
+            per_gemm.append({"name": w.name, "N": w.N, "K": w.K, "type": synth.TYPE_NAME[w.qtype],
+                             "gemm_us": t_main * 1e3, "reduce_us": t_aux * 1e3,
+                             "tflops": 2.0 * M_TOKENS * w.N * w.K / ((t_main + t_aux) * 1e-3) / 1e12})
+    n_launch = max(1, len(gem))
+    achieved = (g_flops / n_launch) / ((g_ms / n_launch) * 1e-3) / 1e12 if g_ms > 0 else None
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        with open(tp) as fh:
+            traffic = json.load(fh).get("k_gemm_cached_bytes_per_launch")
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": P["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": (achieved / P["bf16_tflops"]) if achieved else None, "traffic": traffic,
+                "kernel": "k_gemm_cached (tcgen05 f16 GEMM on the f16 cache)",
+                "peak_kind": f"dense bf16 burst ({P['source']}); f16 nominal rate equals bf16",
+                "frac_of_sustained": (achieved / P["bf16_tflops_sustained"]) if achieved else None,
+                "launches_timed": len(gem), "reduce_ms_per_step": red_ms / args.steps}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_TOKENS, "gemms": [w.name for w in weights],
+                   "weights": "q/k/v/o/gate/up Q4_K, down Q6_K (seeded synthetic blocks, model shapes)",
+                   "gflop_per_step": flops_step / 1e9, "path": "mq_gemm_auto -> cached",
+                   "l2": "inputs larger than L2: 466 MB of f16 weight caches per step vs 126 MB L2",
+                   "parallelism": f"replicas x{world} (independent token batches)"},
+        "tok_per_s_per_layer": world * M_TOKENS / (ms * 1e-3),
+        "tok_per_s_28_layer_gemms_only": world * M_TOKENS / (28 * ms * 1e-3),
+        "frac_of_peak": value / world / P["bf16_tflops"],
+        "roofline": roofline,
+        "per_gemm": per_gemm,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "decode": {"bytes": decode_bytes, "ms": decode_ms,
+                   "gbs": decode_bytes / (decode_ms * 1e-3) / 1e9 if decode_ms else None,
+                   "frac_hbm": (decode_bytes / (decode_ms * 1e-3) / 1e9) / P["hbm_gbs"] if decode_ms else None,
+                   "note": "one-time registration decode of the 7 weights (blocks read + f16 written), cold"},
+    }
+
+    if not args.no_extras:
+        out["e2e"] = e2e_run(mq, torch, weights, handles, xs, ys, stream, min(args.steps, 50), flops_step, dist)
+        out["small_m"] = small_m_sweep(mq, torch, stream, P)
+    if rank == 0 and world == 1 and not args.no_extras:
+        tf, tokens, secs, dsec, threads = oracle_cpu_run(weights, xs, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                               "sample": f"{tokens} of {M_TOKENS} tokens through all 7 GEMMs (f64, {secs:.1f} s); "
+                                         f"oracle decode of the 7 weights took {dsec:.1f} s before"}
+    for h in handles:
+        h.release()
+    if rank == 0:
+        print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_run(mq, torch, weights, handles, xs, ys, stream, steps, flops_step, dist):
+    """Same step through the public API with host buffers: pinned host X
+    copied in, all seven outputs copied back, inside the timed region."""
+    xh = {k: torch.from_numpy(v).pin_memory() for k, v in xs.items()}
+    xd = {k: torch.empty(v.shape, dtype=torch.float16, device="cuda") for k, v in xs.items()}
+    yh = [torch.empty(y.shape, dtype=torch.float32).pin_memory() for y in ys]
+    h2d = sum(v.numel() * 2 for v in xh.values())
+    d2h = sum(y.numel() * 4 for y in ys)
+
+    def step():
+        for k in xh:
+            xd[k].copy_(xh[k], non_blocking=True)
+        for w, h, y in zip(weights, handles, ys):
+            mq.mq_gemm_auto(xd[w.K], h, y, M_TOKENS, stream)
+        for y, yhost in zip(ys, yh):
+            yhost.copy_(y, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": world * flops_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def small_m_sweep(mq, torch, stream, P):
+    """Fused vs cached on the 7B gate (Q4_K 18944x3584) and down (Q6_K
+    3584x18944) shapes, M in {1, 8, 32, 128, 512, 2048}: device time from
+    the library's trace events, cold L2 (a 256 MB buffer is written before
+    each timed call)."""
+    weights, xs = synth.workload("small_m_sweep", seed=0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    res = []
+    for w in weights:
+        if w.name == "up":
+            continue
+        q = torch.from_numpy(w.data).cuda()
+        h = mq.mq_register_weight(w.qtype, q, w.N, w.K)
+        x_all = torch.from_numpy(xs[w.K]).cuda()
+        raw_bytes = synth.nblocks(w.qtype, w.N, w.K) * synth.BLOCK[w.qtype][1]
+        for M in synth.WORKLOADS["small_m_sweep"][1]:
+            x = x_all[:M].contiguous()
+            y = torch.empty((M, w.N), dtype=torch.float32, device="cuda")
+            row = {"name": w.name, "M": M}
+            for path, fn, kind in (("fused", mq.mq_gemm_fused, mq.MQ_TRACE_GEMM_FUSED),
+                                   ("cached", mq.mq_gemm, mq.MQ_TRACE_GEMM_CACHED)):
+                for _ in range(2):
+                    fn(x, h, y, M, stream)
+                ts = []
+                for _ in range(7):
+                    flush.zero_()
+                    mq.mq_trace_enable(True)
+                    fn(x, h, y, M, stream)
+                    torch.cuda.synchronize()
+                    r = mq.mq_trace_records()[-1]
+                    mq.mq_trace_enable(False)
+                    ts.append(r["ms_main"] + r["ms_aux"])
+                t = statistics.median(ts)
+                wbytes = raw_bytes if path == "fused" else 2 * w.N * w.K
+                byts = wbytes + 2 * M * w.K + 4 * M * w.N
+                row[path + "_us"] = t * 1e3
+                row[path + "_tflops"] = 2.0 * M * w.N * w.K / (t * 1e-3) / 1e12
+                row[path + "_gbs"] = byts / (t * 1e-3) / 1e9
+                row[path + "_frac_hbm"] = row[path + "_gbs"] / P["hbm_gbs"]
+            res.append(row)
+        mq.mq_stream_status()
+        h.release()
+    cross = {}
+    for name in ("gate", "down"):
+        ms_ = [r["M"] for r in res if r["name"] == name and r["cached_us"] <= r["fused_us"]]
+        cross[name] = min(ms_) if ms_ else None
+    return {"rows": res, "cached_wins_from_M": cross, "gate_in_use": mq.mq_get_m_gate()}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

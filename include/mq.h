@@ -190,6 +190,33 @@ int mq_stream_status(void *stream);
 /* Number of kernel launches the library has made since load (all kinds). */
 int64_t mq_launch_count(void);
 
+/*
+ * Launch tracing.  While enabled, every mq_gemm / mq_gemm_fused call (and the
+ * decode of mq_register_weight) records CUDA events on the caller's stream
+ * around its main kernel and around its split-K reduce, so the device time
+ * of each kernel can be read back.  No page prints this; it is the library's
+ * own measurement hook.  Calls made while the stream is being captured into
+ * a CUDA graph are not traced.  At most 1 << 16 calls are kept.
+ */
+typedef struct {
+    int32_t kind;      /* MQ_TRACE_* */
+    int32_t type;      /* GGUF type id of the weight */
+    int64_t M, N, K;
+    float ms_main;     /* device time of the GEMM or decode kernel */
+    float ms_aux;      /* device time of the split-K reduce (0 if none) */
+} mq_trace_record;
+
+#define MQ_TRACE_GEMM_CACHED 1
+#define MQ_TRACE_GEMM_FUSED  2
+#define MQ_TRACE_DECODE      3
+
+/* Enable (clears earlier records) or disable recording. */
+int mq_trace_enable(int on);
+/* Number of records kept since the last enable. */
+int64_t mq_trace_count(void);
+/* Read record i (synchronizes its events).  Errors: MQ_ERR_INVALID, MQ_ERR_CUDA. */
+int mq_trace_read(int64_t i, mq_trace_record *out);
+
 /* Static description of a status code. */
 const char *mq_error_string(int status);
 

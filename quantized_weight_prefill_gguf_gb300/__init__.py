@@ -24,7 +24,15 @@ STATUS = {0: "MQ_OK", -1: "MQ_ERR_INVALID", -2: "MQ_ERR_UNSUPPORTED_TYPE", -3: "
 # Every symbol include/mq.h declares.
 EXPORTS = ("mq_register_weight", "mq_release_weight", "mq_weight_info", "mq_dequantize", "mq_gemm",
            "mq_gemm_fused", "mq_gemm_auto", "mq_get_m_gate", "mq_set_m_gate", "mq_reserve_workspace",
-           "mq_stream_status", "mq_launch_count", "mq_error_string", "mq_last_error_detail", "mq_version")
+           "mq_stream_status", "mq_launch_count", "mq_error_string", "mq_last_error_detail", "mq_version",
+           "mq_trace_enable", "mq_trace_count", "mq_trace_read")
+MQ_TRACE_GEMM_CACHED, MQ_TRACE_GEMM_FUSED, MQ_TRACE_DECODE = 1, 2, 3
+
+
+class TraceRecord(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("type", ctypes.c_int32), ("M", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("ms_main", ctypes.c_float),
+                ("ms_aux", ctypes.c_float)]
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -51,6 +59,9 @@ def _load() -> ctypes.CDLL:
         "mq_error_string": ([ctypes.c_int], ctypes.c_char_p),
         "mq_last_error_detail": ([], ctypes.c_char_p),
         "mq_version": ([], ctypes.c_int),
+        "mq_trace_enable": ([ctypes.c_int], ctypes.c_int),
+        "mq_trace_count": ([], _I64),
+        "mq_trace_read": ([_I64, ctypes.POINTER(TraceRecord)], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -200,3 +211,17 @@ def mq_launch_count() -> int:
 
 def mq_version() -> int:
     return int(_lib().mq_version())
+
+
+def mq_trace_enable(on: bool = True) -> None:
+    _check(_lib().mq_trace_enable(1 if on else 0), "mq_trace_enable")
+
+
+def mq_trace_records() -> list[dict]:
+    """All records kept since the last mq_trace_enable(True)."""
+    out = []
+    rec = TraceRecord()
+    for i in range(int(_lib().mq_trace_count())):
+        _check(_lib().mq_trace_read(i, ctypes.byref(rec)), "mq_trace_read")
+        out.append({f: getattr(rec, f) for f, _ in TraceRecord._fields_})
+    return out

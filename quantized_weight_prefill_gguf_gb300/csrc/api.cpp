@@ -15,6 +15,7 @@
 #include <mutex>
 #include <string>
 #include <unordered_set>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -50,6 +51,53 @@ struct DevState {
     int64_t ws_bytes = 0;
 };
 DevState g_dev[kMaxDevices];
+
+// ---------------------------------------------------------------- tracing
+constexpr int64_t kTraceCap = 1 << 16;
+
+struct TraceRec {
+    mq_trace_record r;
+    cudaEvent_t ev[3];
+    bool aux;
+};
+
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;   // grows; events are reused across enables
+int64_t g_trace_n = 0;
+
+// Start a record for a call on stream s; returns its index or -1.
+int64_t trace_begin(cudaStream_t s, int kind, int type, int64_t M, int64_t N, int64_t K)
+{
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (!g_trace_on || g_trace_n >= kTraceCap)
+        return -1;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+        return -1;
+    if (static_cast<int64_t>(g_trace.size()) <= g_trace_n) {
+        TraceRec t{};
+        for (auto &e : t.ev)
+            if (cudaEventCreate(&e) != cudaSuccess)
+                return -1;
+        g_trace.push_back(t);
+    }
+    TraceRec &t = g_trace[g_trace_n];
+    t.r = mq_trace_record{kind, type, M, N, K, 0.f, 0.f};
+    t.aux = false;
+    cudaEventRecord(t.ev[0], s);
+    return g_trace_n++;
+}
+
+void trace_mark(int64_t idx, int which, cudaStream_t s, bool aux = false)
+{
+    if (idx < 0)
+        return;
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    cudaEventRecord(g_trace[idx].ev[which], s);
+    if (which == 2)
+        g_trace[idx].aux = aux;
+}
 
 int fail(int code, const char *fmt, ...)
 {
@@ -230,12 +278,15 @@ int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bo
                 fused ? "fused" : "cached", (long long)M, (long long)w->N, (long long)w->K, plan.bn, plan.tiles,
                 plan.split, plan.full_tiles, plan.units, plan.grid);
 
+    const int64_t tr = trace_begin(s, fused ? MQ_TRACE_GEMM_FUSED : MQ_TRACE_GEMM_CACHED, w->type, M, w->N, w->K);
     cudaError_t e = fused ? mq::launch_gemm_fused(tm_x, a, plan, s) : mq::launch_gemm_cached(w->tm_cache, tm_x, a, plan, s);
     if (e != cudaSuccess)
         return cuda_fail(e, fused ? "fused GEMM launch" : "cached GEMM launch");
+    trace_mark(tr, 1, s);
     e = mq::launch_splitk_reduce(a, plan, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "split-K reduce launch");
+    trace_mark(tr, 2, s, plan.split > 1 && plan.tiles > plan.full_tiles);
     return MQ_OK;
 }
 
@@ -387,7 +438,10 @@ int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, ui
                         (long long)ldk, cudaGetErrorString(e));
         }
         w->cache = static_cast<__half *>(p);
+        const int64_t tr = trace_begin(s, MQ_TRACE_DECODE, type, 0, N, K);
         e = mq::launch_dequant(type, qdata, w->nblocks, w->cache, K, ldk, s);
+        trace_mark(tr, 1, s);
+        trace_mark(tr, 2, s);
         if (e == cudaSuccess && ldk > K)
             e = cudaMemset2DAsync(w->cache + K, static_cast<size_t>(ldk) * 2, 0, static_cast<size_t>(ldk - K) * 2,
                                   static_cast<size_t>(N), s);
@@ -465,10 +519,13 @@ int mq_dequantize(mq_type type, const void *qdata, int64_t N, int64_t K, void *o
     int rc = device_state(&d);
     if (rc)
         return rc;
-    cudaError_t e = mq::launch_dequant(type, qdata, N * K / qk, static_cast<__half *>(out_f16), K, ldo,
-                                       static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t tr = trace_begin(s, MQ_TRACE_DECODE, type, 0, N, K);
+    cudaError_t e = mq::launch_dequant(type, qdata, N * K / qk, static_cast<__half *>(out_f16), K, ldo, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "dequantize launch");
+    trace_mark(tr, 1, s);
+    trace_mark(tr, 2, s);
     return MQ_OK;
 }
 
@@ -526,6 +583,46 @@ int mq_reserve_workspace(int64_t bytes)
         return rc;
     std::lock_guard<std::mutex> lk(g_mu);
     return grow_workspace(*d, bytes);
+}
+
+int mq_trace_enable(int on)
+{
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (on)
+        g_trace_n = 0;
+    g_trace_on = on != 0;
+    return MQ_OK;
+}
+
+int64_t mq_trace_count(void)
+{
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    return g_trace_n;
+}
+
+int mq_trace_read(int64_t i, mq_trace_record *out)
+{
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (!out || i < 0 || i >= g_trace_n)
+        return fail(MQ_ERR_INVALID, "trace record %lld does not exist (count %lld)", (long long)i,
+                    (long long)g_trace_n);
+    TraceRec &t = g_trace[i];
+    cudaError_t e = cudaEventSynchronize(t.ev[2]);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaEventSynchronize(trace)");
+    float a = 0.f, b = 0.f;
+    e = cudaEventElapsedTime(&a, t.ev[0], t.ev[1]);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaEventElapsedTime(trace)");
+    if (t.aux) {
+        e = cudaEventElapsedTime(&b, t.ev[1], t.ev[2]);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaEventElapsedTime(trace)");
+    }
+    *out = t.r;
+    out->ms_main = a;
+    out->ms_aux = b;
+    return MQ_OK;
 }
 
 int mq_stream_status(void *stream)

@@ -1,0 +1,61 @@
+"""Run one GEMM or decode case a few times, for a profiler (ncu) to capture.
+
+    python -m quantized_weight_prefill_gguf_gb300.profile_case \
+        --case fused --type q4_K --N 18944 --K 3584 --M 32 --reps 3
+
+Cases: cached (mq_gemm), fused (mq_gemm_fused), decode (mq_dequantize).
+Inputs are the seeded synthetic blocks of the given shape.  Prints the
+device time of each call from the library's trace events (not valid under a
+profiler, which serialises and replays kernels).
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+import quantized_weight_prefill_gguf_gb300 as mq
+from quantized_weight_prefill_gguf_gb300 import synth
+
+TYPES = {"q4_K": synth.Q4_K, "q6_K": synth.Q6_K, "q8_0": synth.Q8_0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", choices=["cached", "fused", "decode"], required=True)
+    ap.add_argument("--type", choices=sorted(TYPES), default="q4_K")
+    ap.add_argument("--N", type=int, required=True)
+    ap.add_argument("--K", type=int, required=True)
+    ap.add_argument("--M", type=int, default=32)
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--seed", type=int, default=0)
+    args = ap.parse_args(argv)
+
+    qtype = TYPES[args.type]
+    g = synth.rng(args.seed)
+    data = synth.weight_bytes(g, qtype, args.N, args.K)
+    q = torch.from_numpy(data).cuda()
+    if args.case == "decode":
+        out = torch.empty((args.N, args.K), dtype=torch.float16, device="cuda")
+        fn = lambda: mq.mq_dequantize(qtype, q, args.N, args.K, out)  # noqa: E731
+    else:
+        flags = mq.MQ_REG_NO_CACHE if args.case == "fused" else 0
+        h = mq.mq_register_weight(qtype, q, args.N, args.K, flags=flags)
+        x = torch.from_numpy(synth.activations(g, args.M, args.K)).cuda()
+        y = torch.empty((args.M, args.N), dtype=torch.float32, device="cuda")
+        call = mq.mq_gemm_fused if args.case == "fused" else mq.mq_gemm
+        fn = lambda: call(x, h, y, args.M)  # noqa: E731
+    torch.cuda.synchronize()
+    mq.mq_trace_enable(True)
+    for _ in range(args.reps):
+        fn()
+    torch.cuda.synchronize()
+    mq.mq_stream_status()
+    for r in mq.mq_trace_records():
+        print(f"{args.case} {args.type} M={args.M} N={args.N} K={args.K}: "
+              f"{r['ms_main'] * 1e3:.1f} us (+ reduce {r['ms_aux'] * 1e3:.1f} us)")
+    mq.mq_trace_enable(False)
+
+
+if __name__ == "__main__":
+    main()
