@@ -148,8 +148,9 @@ int mq_gemm(const void *x, mq_handle w, float *y, int64_t M, void *stream);
  * quantized bytes and dequantized before the MMA; zero extra VRAM).  The
  * on-chip decode produces the same f16 values as the cache.
  * Extra preconditions: K % 64 == 0 (a 64-element K chunk never straddles a
- * block), and the stream length (N*K/QK blocks times the block bytes) is a
- * multiple of 16 bytes.  Errors as mq_gemm, minus MQ_ERR_NO_CACHE.
+ * block); when K % 256 != 0 (rows start inside blocks) the stream length
+ * (N*K/QK blocks times the block bytes) must also be a multiple of 16 bytes.
+ * Errors as mq_gemm, minus MQ_ERR_NO_CACHE.
  */
 int mq_gemm_fused(const void *x, mq_handle w, float *y, int64_t M, void *stream);
 

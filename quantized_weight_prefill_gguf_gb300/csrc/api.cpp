@@ -31,6 +31,8 @@ struct mq_weight {
     __half *cache;       // null when registered with MQ_REG_NO_CACHE
     int device;
     CUtensorMap tm_cache;
+    int raw_g;           // > 0: the fused path reads raw blocks through raw_maps
+    mq::RawMaps raw_maps;
 };
 
 namespace {
@@ -279,7 +281,10 @@ int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bo
                 plan.split, plan.full_tiles, plan.units, plan.grid);
 
     const int64_t tr = trace_begin(s, fused ? MQ_TRACE_GEMM_FUSED : MQ_TRACE_GEMM_CACHED, w->type, M, w->N, w->K);
-    cudaError_t e = fused ? mq::launch_gemm_fused(tm_x, a, plan, s) : mq::launch_gemm_cached(w->tm_cache, tm_x, a, plan, s);
+    a.raw_g = w->raw_g;
+    a.raw_rb = w->K / w->qk * w->bb;
+    cudaError_t e = fused ? mq::launch_gemm_fused(tm_x, w->raw_maps, a, plan, s)
+                          : mq::launch_gemm_cached(w->tm_cache, tm_x, a, plan, s);
     if (e != cudaSuccess)
         return cuda_fail(e, fused ? "fused GEMM launch" : "cached GEMM launch");
     trace_mark(tr, 1, s);
@@ -425,6 +430,7 @@ int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, ui
     w->qdata = static_cast<const uint8_t *>(qdata);
     w->cache = nullptr;
     w->device = dev;
+    w->raw_g = env_int("MQ_RAW_TMA", 1) ? mq::encode_raw_maps(&w->raw_maps, qdata, type, N, K) : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!(flags & MQ_REG_NO_CACHE)) {
@@ -546,7 +552,7 @@ int mq_gemm_fused(const void *x, mq_handle w, float *y, int64_t M, void *stream)
         return rc;
     if (w->K % 64 != 0)
         return fail(MQ_ERR_SHAPE, "fused path needs K %% 64 == 0 (K=%lld)", (long long)w->K);
-    if ((w->nblocks * w->bb) % 16 != 0)
+    if (w->raw_g == 0 && (w->nblocks * w->bb) % 16 != 0)
         return fail(MQ_ERR_SHAPE, "fused path needs the block stream length (%lld bytes) to be a multiple of 16",
                     (long long)(w->nblocks * w->bb));
     return run_gemm(x, w, y, M, static_cast<cudaStream_t>(stream), true);
@@ -557,7 +563,7 @@ int mq_gemm_auto(const void *x, mq_handle w, float *y, int64_t M, void *stream)
     int rc = check_gemm_args(x, w, y, M);
     if (rc)
         return rc;
-    const bool fused_ok = (w->K % 64 == 0) && ((w->nblocks * w->bb) % 16 == 0);
+    const bool fused_ok = (w->K % 64 == 0) && (w->raw_g > 0 || (w->nblocks * w->bb) % 16 == 0);
     if (!w->cache || (M < current_gate() && fused_ok))
         return mq_gemm_fused(x, w, y, M, stream);
     return mq_gemm(x, w, y, M, stream);

@@ -125,9 +125,9 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *__restrict_
         for (int it = threadIdx.x; it < nb * 4; it += kThreads) {
             const int blk = it >> 2, c = it & 3;
             const uint8_t *b = sm + blk * F::BB;          // 2-byte aligned
-            const float d = f16_bits_to_f32(lds_u16(b));
+            const uint32_t d16 = lds_u16(b);
             const uint32_t w0 = lds_u32_a2(b + 2 + 8 * c), w1 = lds_u32_a2(b + 6 + 8 * c);
-            store8(out, (b0 + blk) * F::QK + 8 * c, K, ldo, q80_eight(d, w0, w1));
+            store8(out, (b0 + blk) * F::QK + 8 * c, K, ldo, q80_eight(d16, w0, w1));
         }
     }
 }

@@ -261,7 +261,13 @@ cudaError_t launch_bn(const CUtensorMap &tw, const CUtensorMap &tx, const GemmAr
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available)
 {
     GemmPlan p{};
-    p.bn = M > 128 ? 256 : (M > 64 ? 128 : (M > 32 ? 64 : 32));
+    // The fused path keeps a whole 256-element K chunk of activations per
+    // stage, so its tiles stop at 128 tokens; at M <= 16 it uses the
+    // narrowest MMA (N = 16), which halves the accumulator traffic per MMA.
+    if (fused)
+        p.bn = M > 64 ? 128 : (M > 32 ? 64 : (M > 16 ? 32 : 16));
+    else
+        p.bn = M > 128 ? 256 : (M > 64 ? 128 : (M > 32 ? 64 : 32));
     // The fused path stages raw weight bytes 256 K-elements (4 K steps) at a
     // time, so its split boundaries fall on multiples of 4 K steps.
     p.kb_align = fused ? 4 : 1;

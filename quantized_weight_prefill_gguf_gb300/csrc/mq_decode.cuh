@@ -13,7 +13,8 @@
 //  * Q6_K: |sc*q6| <= 128*32 = 4096, so d*sc*q6 has <= 23 significant bits
 //    and (d*sc)*q6 is exact in f32.  Q8_0: d*q <= 18 bits, exact.
 //  * The only remaining rounding is f32 -> f16, round to nearest even
-//    (cvt.rn.f16x2.f32), which keeps subnormals and signed zeros.
+//    (cvt.rn.f16x2.f32), which keeps subnormals and signed zeros.  For Q8_0,
+//    where d*q is exact, that single rounding is done by an f16 multiply.
 #pragma once
 
 #include <cstdint>
@@ -57,19 +58,71 @@ __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t
     }
 }
 
+// ---- packed helpers.  Two f32 lanes travel in one 64-bit register so the
+// sm_100-family paired instructions (add/mul/fma .rn.f32x2) do two elements
+// per instruction; each lane rounds exactly like its scalar form.
+
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+// Bytes j and j+1 of v (each 0..255) -> two f32 values 2^23 + byte: the byte
+// permute places the byte under exponent byte 0x4B (0x4B0000bb).
+__device__ __forceinline__ uint64_t magic_pair(uint32_t v, int j)
+{
+    const uint32_t a = __byte_perm(v, 0x4B000000u, 0x7540u | j);
+    const uint32_t b = __byte_perm(v, 0x4B000000u, 0x7540u | (j + 1));
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// Two f32 lanes -> f16x2 (lane 0 in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t cvt_f16x2(uint64_t v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Eight Q4_K outputs of one sub-block: nibbles taken from the 8 bytes held in
 // w0 (bytes 0..3) and w1 (bytes 4..7), low nibbles if sh == 0, high if 4.
 // A = d*sc, B = dmin*m.  Output element j comes from byte j.
+// q = (2^23 + q) - 2^23 exactly, then y = RN16(fma(A, q, -B)).
 __device__ __forceinline__ uint4 q4k_eight(float A, float B, uint32_t w0, uint32_t w1, int sh)
 {
-    float v[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        v[j] = fmaf(A, small_uint_to_f32((w0 >> (8 * j + sh)) & 15u), -B);
-        v[4 + j] = fmaf(A, small_uint_to_f32((w1 >> (8 * j + sh)) & 15u), -B);
-    }
-    return make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]),
-                      pack_f16x2(v[6], v[7]));
+    const uint32_t v0 = (w0 >> sh) & 0x0F0F0F0Fu, v1 = (w1 >> sh) & 0x0F0F0F0Fu;
+    const uint64_t a2 = f32x2(A, A), nb2 = f32x2(-B, -B), m2 = f32x2(-8388608.0f, -8388608.0f);
+    return make_uint4(cvt_f16x2(fma_f32x2(a2, add_f32x2(magic_pair(v0, 0), m2), nb2)),
+                      cvt_f16x2(fma_f32x2(a2, add_f32x2(magic_pair(v0, 2), m2), nb2)),
+                      cvt_f16x2(fma_f32x2(a2, add_f32x2(magic_pair(v1, 0), m2), nb2)),
+                      cvt_f16x2(fma_f32x2(a2, add_f32x2(magic_pair(v1, 2), m2), nb2)));
 }
 
 // Eight Q6_K outputs: low 4 bits from the nibbles of ql bytes (l0 = bytes
@@ -78,30 +131,34 @@ __device__ __forceinline__ uint4 q4k_eight(float A, float B, uint32_t w0, uint32
 __device__ __forceinline__ uint4 q6k_eight(float A, uint32_t l0, uint32_t l1, int lsh, uint32_t h0, uint32_t h1,
                                            int hsh)
 {
-    float v[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t a = ((l0 >> (8 * j + lsh)) & 15u) | (((h0 >> (8 * j + hsh)) & 3u) << 4);
-        const uint32_t b = ((l1 >> (8 * j + lsh)) & 15u) | (((h1 >> (8 * j + hsh)) & 3u) << 4);
-        v[j] = __fmul_rn(A, small_uint_to_f32(a) - 32.0f);
-        v[4 + j] = __fmul_rn(A, small_uint_to_f32(b) - 32.0f);
-    }
-    return make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]),
-                      pack_f16x2(v[6], v[7]));
+    const uint32_t v0 = ((l0 >> lsh) & 0x0F0F0F0Fu) | (((h0 >> hsh) & 0x03030303u) << 4);
+    const uint32_t v1 = ((l1 >> lsh) & 0x0F0F0F0Fu) | (((h1 >> hsh) & 0x03030303u) << 4);
+    const uint64_t a2 = f32x2(A, A), m2 = f32x2(-8388640.0f, -8388640.0f);   // -(2^23 + 32)
+    return make_uint4(cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v0, 0), m2))),
+                      cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v0, 2), m2))),
+                      cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v1, 0), m2))),
+                      cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v1, 2), m2))));
 }
 
-// Eight Q8_0 outputs from 8 int8 quants (w0 bytes 0..3, w1 bytes 4..7).
-// y = RN16(d * q).  (q ^ 0x80) is q + 128 as an unsigned byte.
-__device__ __forceinline__ uint4 q80_eight(float d, uint32_t w0, uint32_t w1)
+// Eight Q8_0 outputs from 8 int8 quants (w0 bytes 0..3, w1 bytes 4..7) and
+// the block's f16 scale bits d16.  d*q is exact in f32, so RN16(RN32(d*q))
+// is RN16(d*q), which the f16x2 multiply computes directly: bytes q+128 are
+// placed under the f16 exponent of 1024 (0x64nn = 1024 + nn), 1152 is
+// subtracted exactly, and the f16 product with d rounds once.
+__device__ __forceinline__ uint32_t q80_pair(uint32_t v, int j, uint32_t d2)
 {
-    float v[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        v[j] = __fmul_rn(d, small_uint_to_f32(((w0 >> (8 * j)) & 0xFFu) ^ 0x80u) - 128.0f);
-        v[4 + j] = __fmul_rn(d, small_uint_to_f32(((w1 >> (8 * j)) & 0xFFu) ^ 0x80u) - 128.0f);
-    }
-    return make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]),
-                      pack_f16x2(v[6], v[7]));
+    const uint32_t h = __byte_perm(v, 0x64646464u, 0x5040u | j | ((j + 1) << 8));
+    uint32_t q, y;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(q) : "r"(h), "r"(0x64806480u));   // 1152 = 0x6480
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(q), "r"(d2));
+    return y;
+}
+
+__device__ __forceinline__ uint4 q80_eight(uint32_t d16, uint32_t w0, uint32_t w1)
+{
+    const uint32_t d2 = (d16 & 0xFFFFu) * 0x10001u;
+    const uint32_t v0 = w0 ^ 0x80808080u, v1 = w1 ^ 0x80808080u;
+    return make_uint4(q80_pair(v0, 0, d2), q80_pair(v0, 2, d2), q80_pair(v1, 0, d2), q80_pair(v1, 2, d2));
 }
 
 }  // namespace mq

@@ -37,7 +37,21 @@ struct GemmArgs {
     int qtype;           // fused path: GGUF type id
     int raw_rs;          // fused path: shared-memory bytes per weight row of a raw stage
     int raw_stages;      // fused path: raw stages in the ring
-    int stages;          // fused path: f16 operand stages in the ring
+    int a_stages;        // fused path: f16 weight-operand stages in the ring
+    int x_stages;        // fused path: activation-tile stages in the ring
+    int raw_g;           // fused path: tensor maps over rows (row classes mod g); 0 = per-row bulk copies
+    int64_t raw_rb;      // fused path: bytes per weight row (when rows start on block boundaries)
+};
+
+// Raw-weight tensor maps of a weight whose rows start on block boundaries
+// (K % 256 == 0): row n is RB = K/QK*bytes bytes long.  When RB is not a
+// multiple of 16 (Q6_K), only every g-th row starts 16-byte aligned, so map
+// c (c < g) covers the rows n = c + g*i with row stride g*RB and a base
+// aligned down by (c*RB) % 16.  Elements are u16; a box is one 256-element
+// chunk (plus the misalignment) of 128/g rows.
+constexpr int kMaxRawMaps = 8;
+struct RawMaps {
+    CUtensorMap m[kMaxRawMaps];
 };
 
 struct GemmPlan {
@@ -62,8 +76,14 @@ int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fuse
 cudaError_t launch_gemm_cached(const CUtensorMap &tm_w, const CUtensorMap &tm_x, const GemmArgs &a,
                                const GemmPlan &p, cudaStream_t s);
 
-// Fused path: tm_x as above; the weight is read from a.wq.
-cudaError_t launch_gemm_fused(const CUtensorMap &tm_x, const GemmArgs &a, const GemmPlan &p, cudaStream_t s);
+// Fused path: tm_x as above; the weight is read from a.wq, through `maps`
+// when a.raw_g > 0.
+cudaError_t launch_gemm_fused(const CUtensorMap &tm_x, const RawMaps &maps, const GemmArgs &a, const GemmPlan &p,
+                              cudaStream_t s);
+
+// Build the raw-weight tensor maps of a block-aligned weight; returns g (0
+// when the weight does not qualify: K % 256 != 0).
+int encode_raw_maps(RawMaps *maps, const void *qdata, int type, int64_t N, int64_t K);
 
 // Fixed-order sum of the split-K partial planes into Y.
 cudaError_t launch_splitk_reduce(const GemmArgs &a, const GemmPlan &p, cudaStream_t s);

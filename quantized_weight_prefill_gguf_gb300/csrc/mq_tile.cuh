@@ -51,8 +51,9 @@ __device__ __forceinline__ UnitInfo unit_info(const GemmArgs &a, int u)
 // reads it 32 columns (tokens) at a time and stores: Y[m, n] for a whole
 // tile, the partial plane ws[slot][part][col][row] for a split unit.  In
 // both cases the 32 lanes of a store instruction write 32 consecutive
-// floats.  Then it hands the accumulator back to the MMA warp.
-template <int BN>
+// floats.  Then it hands the accumulator back to the MMA warp.  NACC
+// accumulators of BN columns each sit at TMEM columns 0, BN, ...
+template <int BN, int NACC = 2>
 __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, uint64_t *tfull, uint64_t *tempty,
                                               volatile int *abort_flag, int warp, int lane)
 {
@@ -68,25 +69,32 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
         tc_fence_after();
         const int64_t n = static_cast<int64_t>(ui.tile / a.m_tiles) * kTileRows + row;
         const int64_t m0 = static_cast<int64_t>(ui.tile % a.m_tiles) * BN;
+        constexpr int kCols = BN < 32 ? BN : 32;   // columns per TMEM load
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < BN; c += kCols) {
             uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + c), r);
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + c);
+            if constexpr (kCols == 32) {
+                tmem_ld_32x32b_x32(taddr, r);
+            } else {
+                uint32_t (&r16)[16] = *reinterpret_cast<uint32_t (*)[16]>(r);
+                tmem_ld_32x32b_x16(taddr, r16);
+            }
             tmem_ld_wait();
             if (ui.part < 0) {
                 if (n < a.N) {
                     float *yp = a.y + (m0 + c) * a.N + n;
                     const int64_t rem = a.M - (m0 + c);
-                    const int lim = rem < 32 ? static_cast<int>(rem) : 32;
+                    const int lim = rem < kCols ? static_cast<int>(rem) : kCols;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
+                    for (int j = 0; j < kCols; ++j)
                         if (j < lim)
                             yp[static_cast<int64_t>(j) * a.N] = __uint_as_float(r[j]);
                 }
             } else {
                 float *wp = a.ws + ((static_cast<int64_t>(ui.slot) * a.split + ui.part) * BN + c) * kTileRows + row;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
+                for (int j = 0; j < kCols; ++j)
                     wp[j * kTileRows] = __uint_as_float(r[j]);
             }
         }
@@ -94,7 +102,7 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
         __syncwarp();
         if (lane == 0)
             mbar_arrive(&tempty[acc]);
-        if (++acc == 2) {
+        if (++acc == NACC) {
             acc = 0;
             acc_phase ^= 1u;
         }

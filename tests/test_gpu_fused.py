@@ -133,3 +133,23 @@ def test_gate_dispatch(orc):
                 assert_gemm_close(y, y_ref, f"auto M={M}")
     finally:
         mq.mq_set_m_gate(old)
+
+
+@pytest.mark.parametrize("qtype,N,K", [(synth.Q4_K, 256, 1024), (synth.Q6_K, 136, 1536), (synth.Q8_0, 128, 768)])
+def test_raw_paths_agree(orc, qtype, N, K, monkeypatch):
+    """Block-aligned weights are read through row-class tensor maps; with
+    MQ_RAW_TMA=0 the same weight takes the per-row bulk-copy path.  Both
+    must decode to the oracle's values (one-hot identity)."""
+    mq = _mq()
+    g = synth.rng(N * 7 + K)
+    data = synth.weight_bytes(g, qtype, N, K)
+    q = dev(data)
+    W = orc.f16_to_f32(orc.decode_matrix(qtype, data, N, K))
+    x = dev(np.eye(K, dtype=np.float16))
+    h_tma = mq.mq_register_weight(qtype, q, N, K, flags=mq.MQ_REG_NO_CACHE)
+    monkeypatch.setenv("MQ_RAW_TMA", "0")
+    h_bulk = mq.mq_register_weight(qtype, q, N, K, flags=mq.MQ_REG_NO_CACHE)
+    monkeypatch.delenv("MQ_RAW_TMA")
+    for h in (h_tma, h_bulk):
+        y = run(mq.mq_gemm_fused, x, h, K, N)
+        assert np.array_equal(y, W.T)
