@@ -23,6 +23,7 @@ Printed: one JSON line (rank 0) with the contract keys plus
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -57,8 +58,33 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def cached_kernel_source_hash() -> str:
+    """sha256 over the sources that make up the cached GEMM kernel."""
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "mq_tile.cuh", "mq_ptx.cuh"):
+        with open(os.path.join(ROOT, "quantized_weight_prefill_gguf_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def layer_flops(weights, M):
     return sum(2.0 * M * w.N * w.K for w in weights)
+
+
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest x over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_step: float, ms_per_step: float) -> float:
+    """Weak scaling: every rank runs its own step, the job does world steps
+    in the slowest rank's time."""
+    return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
 
 
 # ---------------------------------------------------------------- clocks
@@ -273,14 +299,10 @@ def main():
     launches = mq.mq_launch_count() - launches0
     clk = clocks.stop()
     mq.mq_stream_status()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dist, "cuda")
 
     flops_step = layer_flops(weights, M_TOKENS)
-    value = world * flops_step / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, ms)
 
     # ---- roofline of the dominant kernel: the cached GEMM (k_gemm_cached)
     recs = mq.mq_trace_records()
@@ -300,10 +322,13 @@ def main():
     n_launch = max(1, len(gem))
     achieved = (g_flops / n_launch) / ((g_ms / n_launch) * 1e-3) / 1e12 if g_ms > 0 else None
     traffic = None
-    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    tp = os.path.join(ROOT, "profiles", "k_gemm_cached.qwen2.5-7b_layer.traffic.json")
     if os.path.exists(tp):
         with open(tp) as fh:
-            traffic = json.load(fh).get("k_gemm_cached_bytes_per_launch")
+            rec = json.load(fh)
+        # the counters only describe the kernel source they were taken from
+        if rec.get("kernel_source_sha256") == cached_kernel_source_hash():
+            traffic = rec.get("k_gemm_cached_bytes_per_launch")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": P["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": (achieved / P["bf16_tflops"]) if achieved else None, "traffic": traffic,
                 "kernel": "k_gemm_cached (tcgen05 f16 GEMM on the f16 cache)",
@@ -378,13 +403,9 @@ def e2e_run(mq, torch, weights, handles, xs, ys, stream, steps, flops_step, dist
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, dist, "cuda")
     world = dist.get_world_size() if dist is not None else 1
-    return {"value": world * flops_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+    return {"value": whole_job_tflops(world, flops_step, ms), "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
 

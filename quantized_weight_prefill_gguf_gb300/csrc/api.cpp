@@ -283,6 +283,10 @@ int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bo
     const int64_t tr = trace_begin(s, fused ? MQ_TRACE_GEMM_FUSED : MQ_TRACE_GEMM_CACHED, w->type, M, w->N, w->K);
     a.raw_g = w->raw_g;
     a.raw_rb = w->K / w->qk * w->bb;
+    // Failure injection for tests: the weight producer issues nothing, the
+    // kernel's bounded waits run out (about 1 s), it exits cleanly and
+    // mq_stream_status() reports MQ_ERR_DEVICE.
+    a.stall_producer = env_int("MQ_INJECT_PRODUCER_STALL", 0) != 0 ? 1 : 0;
     cudaError_t e = fused ? mq::launch_gemm_fused(tm_x, w->raw_maps, a, plan, s)
                           : mq::launch_gemm_cached(w->tm_cache, tm_x, a, plan, s);
     if (e != cudaSuccess)

@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         int r = 0;
         uint32_t rphase = 0;
         uint32_t issued = 0, iparity = 0;
-        bool ok = true;
+        bool ok = a.stall_producer == 0;
         for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
             const UnitInfo ui = unit_info(a, u);
             const int64_t n0 = static_cast<int64_t>(ui.tile / a.m_tiles) * kTileRows;

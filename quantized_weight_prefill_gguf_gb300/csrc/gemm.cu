@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issue_parity = 0;   // per-stage: load in flight, its phase parity
-            bool ok = true;
+            bool ok = a.stall_producer == 0;
             for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
                 const UnitInfo ui = unit_info(a, u);
                 const int n0 = (ui.tile / a.m_tiles) * kTileRows;

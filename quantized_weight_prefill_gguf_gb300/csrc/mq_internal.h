@@ -41,6 +41,8 @@ struct GemmArgs {
     int x_stages;        // fused path: activation-tile stages in the ring
     int raw_g;           // fused path: tensor maps over rows (row classes mod g); 0 = per-row bulk copies
     int64_t raw_rb;      // fused path: bytes per weight row (when rows start on block boundaries)
+    int stall_producer;  // failure-injection hook: the weight producer issues nothing, so the
+                         // consumers' bounded waits run out (tests of the timeout path)
 };
 
 // Raw-weight tensor maps of a weight whose rows start on block boundaries

@@ -128,3 +128,35 @@ def test_dependent_chain_and_graph_capture(orc):
     torch.cuda.synchronize()
     mq.mq_stream_status()
     assert torch.equal(y2, ref2)
+
+
+@pytest.mark.parametrize("path", ["cached", "fused"])
+def test_bounded_wait_timeout_recovers(orc, monkeypatch, path):
+    """A producer that never delivers (injected from the host): every
+    consumer's bounded wait runs out after about a second, the kernel exits
+    cleanly (TMEM freed), mq_stream_status reports MQ_ERR_DEVICE, and the
+    context stays usable -- the next call is correct.  No GPU fault."""
+    import time
+    torch = torch_cuda()
+    mq = _mq()
+    g = synth.rng(12)
+    N, K, M = 256, 512, 48
+    data = synth.weight_bytes(g, synth.Q4_K, N, K)
+    x = dev(synth.activations(g, M, K))
+    h = mq.mq_register_weight(synth.Q4_K, dev(data), N, K)
+    fn = mq.mq_gemm if path == "cached" else mq.mq_gemm_fused
+    y = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    mq.mq_stream_status()
+    monkeypatch.setenv("MQ_INJECT_PRODUCER_STALL", "1")
+    t0 = time.time()
+    fn(x, h, y, M)
+    with pytest.raises(mq.MQError) as ei:
+        mq.mq_stream_status()
+    assert ei.value.code == -8 and "timed out" in str(ei.value)
+    assert time.time() - t0 < 60
+    monkeypatch.delenv("MQ_INJECT_PRODUCER_STALL")
+    mq.mq_stream_status()   # status word was cleared by the failing read
+    fn(x, h, y, M)
+    mq.mq_stream_status()
+    y_ref = orc.gemm_f64(x.cpu().numpy().view(np.uint16), orc.decode_matrix(synth.Q4_K, data, N, K))
+    assert_gemm_close(y.cpu().numpy(), y_ref, f"{path} after a timed-out call")
