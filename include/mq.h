@@ -162,6 +162,32 @@ int mq_gemm_fused(const void *x, mq_handle w, float *y, int64_t M, void *stream)
  */
 int mq_gemm_auto(const void *x, mq_handle w, float *y, int64_t M, void *stream);
 
+/*
+ * mq_gemm_noalloc -- the cached GEMM (same result as mq_gemm, same
+ * arguments) for callers that cannot allocate device memory: code that runs
+ * while a stream is captured into a CUDA graph in global capture mode (where
+ * cudaMalloc is refused), engines whose own pool owns the device's memory and
+ * forbids other allocations, and latency-critical paths that must not risk
+ * the implicit synchronization an allocation or a free can cause.  mq_gemm
+ * may grow its split-K scratch with cudaMalloc on first use; this entry point
+ * never calls cudaMalloc, cudaFree or any allocating routine.  No page
+ * describes it: it is this library's own addition.
+ *
+ * Its split-K scratch is one 16 MiB file-scope device array, which every GPU
+ * that loads this library holds until the process exits.  A call whose split
+ * plan needs more than 16 MiB fails with MQ_ERR_SHAPE and says so (at
+ * M = 2048 that is the case for a 3584-row weight, for example).  The first
+ * call on each device looks up the array's device address (with that device
+ * current); make that first call before any stream capture.  All calls share
+ * the array, so calls that overlap on the GPU (different streams, or graphs
+ * replayed concurrently) race and must be serialized by the caller.  Every
+ * call overwrites all the scratch it reads, so nothing needs clearing between
+ * calls.  Device-side timeouts of these calls are reported by
+ * mq_stream_status (whose own first call on a device does allocate).
+ * Errors: as mq_gemm, plus MQ_ERR_SHAPE when the scratch is too small.
+ */
+int mq_gemm_noalloc(const void *x, mq_handle w, float *y, int64_t M, void *stream);
+
 /* Current M gate and a setter (value >= 1). */
 int64_t mq_get_m_gate(void);
 int mq_set_m_gate(int64_t m);

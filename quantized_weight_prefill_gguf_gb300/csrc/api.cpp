@@ -351,6 +351,75 @@ CUresult encode_f16_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+int set_error(int code, const char *what, cudaError_t e)
+{
+    if (e != cudaSuccess)
+        return fail(code, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+    return fail(code, "%s", what);
+}
+
+// The cached GEMM with caller-provided split-K scratch and status word; it
+// allocates nothing (no device_state(), no workspace growth).  Rejects a
+// problem whose split-K plan needs more than scratch_bytes.
+int gemm_cached_into_scratch(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, float *scratch,
+                             int64_t scratch_bytes, unsigned *status)
+{
+    int rc = check_gemm_args(x, w, y, M);
+    if (rc)
+        return rc;
+    if (!w->cache)
+        return fail(MQ_ERR_NO_CACHE, "weight was registered with MQ_REG_NO_CACHE; this entry point reads the f16 cache");
+    int dev = 0, sms = 0, major = 0, minor = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    if (major != 10 || minor != 3)
+        return fail(MQ_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
+    if (dev != w->device)
+        return fail(MQ_ERR_INVALID, "weight was registered on device %d, current device is %d", w->device, dev);
+    const int64_t want = plan_ws_bytes_wanted(M, w->N, w->K, sms, false);
+    if (want > scratch_bytes)
+        return fail(MQ_ERR_SHAPE,
+                    "M=%lld N=%lld K=%lld needs %lld bytes of split-K scratch; the static scratch holds %lld bytes",
+                    (long long)M, (long long)w->N, (long long)w->K, (long long)want, (long long)scratch_bytes);
+    const GemmPlan plan = plan_gemm(M, w->N, w->K, sms, false, scratch_bytes);
+
+    CUtensorMap tm_x;
+    CUresult cr = encode_f16_2d(&tm_x, x, M, w->K, w->K, 64, plan.bn);
+    if (cr != CUDA_SUCCESS)
+        return fail(MQ_ERR_CUDA, "tensor map for x (M=%lld, K=%lld, box 64x%d): CUresult %d", (long long)M,
+                    (long long)w->K, plan.bn, (int)cr);
+    GemmArgs a{};
+    a.y = y;
+    a.ws = scratch;
+    a.status = status;
+    a.wq = w->qdata;
+    a.M = M;
+    a.N = w->N;
+    a.K = w->K;
+    a.m_tiles = static_cast<int>((M + plan.bn - 1) / plan.bn);
+    a.n_tiles = static_cast<int>((w->N + 127) / 128);
+    a.kblocks = static_cast<int>((w->K + 63) / 64);
+    a.full_tiles = plan.full_tiles;
+    a.split = plan.split;
+    a.units = plan.units;
+    a.kb_align = plan.kb_align;
+    a.qtype = w->type;
+    e = launch_gemm_cached(w->tm_cache, tm_x, a, plan, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cached GEMM launch");
+    e = launch_splitk_reduce(a, plan, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "split-K reduce launch");
+    return MQ_OK;
+}
+
 }  // namespace mq
 
 extern "C" {
@@ -648,6 +717,7 @@ int mq_stream_status(void *stream)
     e = cudaMemcpy(&st, d->status, sizeof st, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess)
         return cuda_fail(e, "reading the device status word");
+    st |= mq::noalloc_take_status();
     if (st != 0) {
         cudaMemset(d->status, 0, sizeof st);
         return fail(MQ_ERR_DEVICE, "device status 0x%x:%s%s", st, (st & 1u) ? " pipeline wait timed out" : "",

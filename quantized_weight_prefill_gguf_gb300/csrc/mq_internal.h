@@ -7,6 +7,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+struct mq_weight;   // the C ABI's handle type (include/mq.h)
+
 namespace mq {
 
 // Counts every kernel launch the library makes (reported by mq_launch_count).
@@ -89,6 +91,20 @@ int encode_raw_maps(RawMaps *maps, const void *qdata, int type, int64_t N, int64
 
 // Fixed-order sum of the split-K partial planes into Y.
 cudaError_t launch_splitk_reduce(const GemmArgs &a, const GemmPlan &p, cudaStream_t s);
+
+// The cached GEMM into caller-provided split-K scratch and status word,
+// allocating nothing; MQ_ERR_SHAPE when the plan needs more than
+// scratch_bytes.  Used by mq_gemm_noalloc.
+int gemm_cached_into_scratch(const void *x, ::mq_weight *w, float *y, int64_t M, cudaStream_t s, float *scratch,
+                             int64_t scratch_bytes, unsigned *status);
+
+// Record `code` with a detail message (what, and the CUDA error if any) for
+// mq_last_error_detail(); returns code.
+int set_error(int code, const char *what, cudaError_t e);
+
+// Read and clear the status word of mq_gemm_noalloc calls on the current
+// device (0 when that entry point was never set up there).
+unsigned noalloc_take_status();
 
 // ---------------------------------------------------------------- tensor maps
 // Encode a 2-D f16 row-major [rows, cols] tensor map with row stride `ld`
