@@ -16,9 +16,19 @@
 // stops its vector loads at the stream's end and finishes with byte loads,
 // so nothing past the stream is read.
 //
+// Work split.  A CTA owns a span of G whole blocks.  Each warp decodes
+// kPasses groups of blocks; in a group the 32 lanes cover whole blocks and
+// every lane produces 16 elements from one scale computation, written as two
+// 16-byte stores.  The lanes are paired so that the two lanes of a pair
+// write the two halves of one 32-byte sector in the same store instruction:
+// a store instruction of the warp writes 16 complete sectors.
+//
 // Output: element (n,k) of the flat stream (flat index n*K+k) goes to
-// out[n*ldo + k], eight elements (16 bytes) per store.  K % 8 == 0 keeps a
-// group of eight inside one row.
+// out[n*ldo + k].  Three addressing cases, uniform per launch: ldo == K (the
+// flat index is the address); K a multiple of the block length (a block lies
+// in one row, its row comes from one multiply-high division per block); any
+// other K (K % 8 == 0 keeps a group of eight inside one row; one division
+// per group of eight).
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -30,41 +40,72 @@ namespace mq {
 namespace {
 
 template <int T> struct Fmt;
-template <> struct Fmt<8> { static constexpr int QK = 32, BB = 34, G = 256; };    // span 8704 B
-template <> struct Fmt<12> { static constexpr int QK = 256, BB = 144, G = 64; };  // span 9216 B
-template <> struct Fmt<14> { static constexpr int QK = 256, BB = 210, G = 64; };  // span 13440 B
+// QK elements per block, BB bytes per block, BPG blocks per lane group, G
+// blocks per CTA span (G * BB is a multiple of 16).
+template <> struct Fmt<8> { static constexpr int QK = 32, BB = 34, BPG = 16, G = 256; };    // span 8704 B
+template <> struct Fmt<12> { static constexpr int QK = 256, BB = 144, BPG = 2, G = 32; };   // span 4608 B
+template <> struct Fmt<14> { static constexpr int QK = 256, BB = 210, BPG = 2, G = 32; };   // span 6720 B
 
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 
-__device__ __forceinline__ uint32_t lds_u16(const uint8_t *p)
+// Row/column of a block index: q = x / d by multiply-high with
+// m = floor((2^32 - 1) / d), which undershoots the quotient by at most 2 for
+// x < 2^32, then at most two corrections.
+struct BlockRows {
+    uint32_t bpr, m;
+};
+
+__device__ __forceinline__ void block_row(uint32_t x, BlockRows br, uint32_t &q, uint32_t &r)
 {
-    return *reinterpret_cast<const uint16_t *>(p);
+    q = __umulhi(x, br.m);
+    r = x - q * br.bpr;
+    if (r >= br.bpr) { ++q; r -= br.bpr; }
+    if (r >= br.bpr) { ++q; r -= br.bpr; }
 }
 
-// Little-endian 32-bit word from two 2-byte-aligned shared loads.
-__device__ __forceinline__ uint32_t lds_u32_a2(const uint8_t *p)
+// Eight consecutive bytes of the staged span at a 2-byte-aligned offset, as
+// two little-endian words: three aligned word loads and a funnel shift.
+// May read up to 4 bytes past the eight (the span buffer is padded).
+__device__ __forceinline__ uint2 lds8_a2(const uint8_t *sm, int off)
 {
-    return lds_u16(p) | (lds_u16(p + 2) << 16);
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(sm) + (off >> 2);
+    const uint32_t sh = static_cast<uint32_t>(off & 2) * 8u;
+    const uint32_t t0 = w[0], t1 = w[1], t2 = w[2];
+    return make_uint2(__funnelshift_r(t0, t1, sh), __funnelshift_r(t1, t2, sh));
 }
 
-__device__ __forceinline__ void store8(__half *out, int64_t flat, int64_t K, int64_t ldo, uint4 v)
+__device__ __forceinline__ uint32_t lds_u16(const uint8_t *sm, int off)
 {
-    __half *dst;
-    if (ldo == K) {
-        dst = out + flat;
-    } else {
-        const int64_t n = flat / K;
-        dst = out + n * ldo + (flat - n * K);
+    return *reinterpret_cast<const uint16_t *>(sm + off);
+}
+
+// Destination of element e of block bi.  mode 0: ldo == K; mode 1: K is a
+// multiple of QK; mode 2: general (e and e+7 in the same row).
+template <int QK>
+__device__ __forceinline__ __half *dest(__half *out, uint32_t bi, int e, int mode, int64_t K, int64_t ldo,
+                                        BlockRows br)
+{
+    if (mode == 0)
+        return out + static_cast<int64_t>(bi) * QK + e;
+    if (mode == 1) {
+        uint32_t n, c;
+        block_row(bi, br, n, c);
+        return out + static_cast<int64_t>(n) * ldo + static_cast<int64_t>(c) * QK + e;
     }
-    stg_v4(dst, v);
+    const int64_t f = static_cast<int64_t>(bi) * QK + e;
+    const int64_t n = f / K;
+    return out + n * ldo + (f - n * K);
 }
 
 template <int T>
 __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *__restrict__ q, int64_t nblocks,
-                                                      __half *__restrict__ out, int64_t K, int64_t ldo)
+                                                      __half *__restrict__ out, int64_t K, int64_t ldo, int mode,
+                                                      BlockRows br)
 {
     using F = Fmt<T>;
-    __shared__ __align__(16) uint8_t sm[F::G * F::BB];
+    constexpr int kPasses = F::G / (kWarps * F::BPG);
+    __shared__ __align__(16) uint8_t sm[F::G * F::BB + 16];
 
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * F::G;
     const int nb = static_cast<int>(nblocks - b0 < F::G ? nblocks - b0 : F::G);
@@ -77,57 +118,92 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *__restrict_
         sm[i] = src[i];
     __syncthreads();
 
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if constexpr (T == 12) {
-        // 16 items per block: qs bytes [32p+i0, 32p+i0+8) feed elements
-        // 64p+i0.. (low nibbles, sub-block 2p) and 64p+32+i0.. (high, 2p+1).
-        for (int it = threadIdx.x; it < nb * 16; it += kThreads) {
-            const int blk = it >> 4, sub = it & 15;
-            const int p = sub >> 2, i0 = (sub & 3) * 8;
-            const uint8_t *b = sm + blk * F::BB;          // 16-byte aligned
-            const uint32_t h = *reinterpret_cast<const uint32_t *>(b);
-            const float d = f16_bits_to_f32(h), dmin = f16_bits_to_f32(h >> 16);
-            const uint32_t s0 = *reinterpret_cast<const uint32_t *>(b + 4);
-            const uint32_t s1 = *reinterpret_cast<const uint32_t *>(b + 8);
-            const uint32_t s2 = *reinterpret_cast<const uint32_t *>(b + 12);
-            const uint2 qw = *reinterpret_cast<const uint2 *>(b + 16 + 32 * p + i0);
-            int sc, m;
-            q4k_scale_min(s0, s1, s2, 2 * p, sc, m);
-            const uint4 lo = q4k_eight(__fmul_rn(d, (float)sc), __fmul_rn(dmin, (float)m), qw.x, qw.y, 0);
-            q4k_scale_min(s0, s1, s2, 2 * p + 1, sc, m);
-            const uint4 hi = q4k_eight(__fmul_rn(d, (float)sc), __fmul_rn(dmin, (float)m), qw.x, qw.y, 4);
-            const int64_t f = (b0 + blk) * F::QK + 64 * p + i0;
-            store8(out, f, K, ldo, lo);
-            store8(out, f + 32, K, ldo, hi);
+        // Lane pair (2j, 2j+1) of a 16-lane half owns sub-block s = j of one
+        // block: 32 elements with one (scale, min); lane h = 0/1 of the pair
+        // takes elements 32s + 8h + {0..7} and 32s + 16 + 8h + {0..7}, whose
+        // nibbles sit in qs bytes 32(s/2) + 8h and +16 (low nibbles for even
+        // s, high for odd).
+        const int l = lane & 15, sub = l >> 1, h = l & 1;
+        const int nsh = (sub & 1) * 4;
+        const int bsel = (sub & 3) * 8;                 // byte j = s mod 4 of the scale words
+        const bool upper = sub >= 4;
+        const int qoff = 16 + 32 * (sub >> 1) + 8 * h;
+        const int eoff = 32 * sub + 8 * h;
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+            const int blk = (warp * kPasses + ps) * F::BPG + (lane >> 4);
+            if (blk < nb) {
+                const uint8_t *b = sm + blk * F::BB;    // 16-byte aligned
+                const uint4 hd = *reinterpret_cast<const uint4 *>(b);
+                const uint2 w0 = *reinterpret_cast<const uint2 *>(b + qoff);
+                const uint2 w1 = *reinterpret_cast<const uint2 *>(b + qoff + 16);
+                // 6-bit scale and min of sub-block s from the 12 scale bytes
+                // (words hd.y, hd.z, hd.w): for s < 4 the low 6 bits of
+                // bytes s and s+4; for s >= 4 the nibbles of byte s+4 with
+                // the top two bits of bytes s-4 and s on top.
+                const uint32_t a = (hd.y >> bsel) & 0xFFu, bm = (hd.z >> bsel) & 0xFFu, c = (hd.w >> bsel) & 0xFFu;
+                const uint32_t sc = upper ? ((c & 15u) | ((a >> 2) & 0x30u)) : (a & 63u);
+                const uint32_t mn = upper ? ((c >> 4) | ((bm >> 2) & 0x30u)) : (bm & 63u);
+                const float A = __fmul_rn(f16_bits_to_f32(hd.x), small_uint_to_f32(sc));
+                const float B = __fmul_rn(f16_bits_to_f32(hd.x >> 16), small_uint_to_f32(mn));
+                const uint4 y0 = q4k_eight(A, B, w0.x, w0.y, nsh);
+                const uint4 y1 = q4k_eight(A, B, w1.x, w1.y, nsh);
+                const uint32_t bi = static_cast<uint32_t>(b0 + blk);
+                stg_v4(dest<F::QK>(out, bi, eoff, mode, K, ldo, br), y0);
+                stg_v4(dest<F::QK>(out, bi, eoff + 16, mode, K, ldo, br), y1);
+            }
         }
     } else if constexpr (T == 14) {
-        // 8 items per block: half h, l0 in {0,8,16,24}: ql bytes 64h+l0..
-        // and 64h+32+l0.., qh bytes 32h+l0.. feed the four quarters t of the
-        // half, elements 128h + 32t + l0 .. +8 with scale sc[8h + 2t + l0/16].
-        for (int it = threadIdx.x; it < nb * 8; it += kThreads) {
-            const int blk = it >> 3, sub = it & 7;
-            const int hh = sub >> 2, l0 = (sub & 3) * 8;
-            const uint8_t *b = sm + blk * F::BB;          // 2-byte aligned
-            const uint8_t *ql = b + 64 * hh + l0;
-            const uint8_t *qh = b + 128 + 32 * hh + l0;
-            const uint32_t la0 = lds_u32_a2(ql), la1 = lds_u32_a2(ql + 4);
-            const uint32_t lb0 = lds_u32_a2(ql + 32), lb1 = lds_u32_a2(ql + 36);
-            const uint32_t h0 = lds_u32_a2(qh), h1 = lds_u32_a2(qh + 4);
-            const float d = f16_bits_to_f32(lds_u16(b + 208));
-            const int8_t *sc = reinterpret_cast<const int8_t *>(b + 192 + 8 * hh + (l0 >> 4));
-            const int64_t f = (b0 + blk) * F::QK + 128 * hh + l0;
-            store8(out, f, K, ldo, q6k_eight(__fmul_rn(d, (float)sc[0]), la0, la1, 0, h0, h1, 0));
-            store8(out, f + 32, K, ldo, q6k_eight(__fmul_rn(d, (float)sc[2]), lb0, lb1, 0, h0, h1, 2));
-            store8(out, f + 64, K, ldo, q6k_eight(__fmul_rn(d, (float)sc[4]), la0, la1, 4, h0, h1, 4));
-            store8(out, f + 96, K, ldo, q6k_eight(__fmul_rn(d, (float)sc[6]), lb0, lb1, 4, h0, h1, 6));
+        // Lane pair j of a 16-lane half owns the 32 elements 128hh + 32t + l
+        // (l = 0..31) with hh = j/4, t = j%4; lane h of the pair takes l in
+        // 8h + {0..7} (scale byte 8hh + 2t) and 16 + 8h + {0..7} (scale
+        // byte 8hh + 2t + 1).  Low nibbles: ql bytes 64hh + 32(t%2) + l,
+        // shifted by 4(t/2); high bits: qh bytes 32hh + l, bits 2t, 2t+1.
+        const int l = lane & 15, grp = l >> 1, h = l & 1;
+        const int hh = grp >> 2, t = grp & 3;
+        const int lsh = (t >> 1) * 4, hrot = (2 * t + 28) & 31;
+        const int qloff = 64 * hh + 32 * (t & 1) + 8 * h;
+        const int qhoff = 128 + 32 * hh + 8 * h;
+        const int scoff = 192 + 8 * hh + 2 * t;
+        const int eoff = 128 * hh + 32 * t + 8 * h;
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+            const int blk = (warp * kPasses + ps) * F::BPG + (lane >> 4);
+            if (blk < nb) {
+                const int bo = blk * F::BB;             // 2-byte aligned
+                const uint2 l0 = lds8_a2(sm, bo + qloff), l1 = lds8_a2(sm, bo + qloff + 16);
+                const uint2 h0 = lds8_a2(sm, bo + qhoff), h1 = lds8_a2(sm, bo + qhoff + 16);
+                const float d = f16_bits_to_f32(lds_u16(sm, bo + 208));
+                // Two int8 scales: biased to 0..255 by flipping the sign bit,
+                // converted exactly with the 2^23 trick, unbiased, times d.
+                const uint64_t s2 = add_f32x2(magic_pair(lds_u16(sm, bo + scoff) ^ 0x8080u, 0),
+                                              f32x2(-8388736.0f, -8388736.0f));   // -(2^23 + 128)
+                float A0, A1;
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(A0), "=f"(A1) : "l"(mul_f32x2(s2, f32x2(d, d))));
+                const uint4 y0 = q6k_core(A0, q6k_bytes(l0.x, lsh, h0.x, hrot), q6k_bytes(l0.y, lsh, h0.y, hrot));
+                const uint4 y1 = q6k_core(A1, q6k_bytes(l1.x, lsh, h1.x, hrot), q6k_bytes(l1.y, lsh, h1.y, hrot));
+                const uint32_t bi = static_cast<uint32_t>(b0 + blk);
+                stg_v4(dest<F::QK>(out, bi, eoff, mode, K, ldo, br), y0);
+                stg_v4(dest<F::QK>(out, bi, eoff + 16, mode, K, ldo, br), y1);
+            }
         }
     } else {
-        // 4 items per block: quants 8c..8c+7.
-        for (int it = threadIdx.x; it < nb * 4; it += kThreads) {
-            const int blk = it >> 2, c = it & 3;
-            const uint8_t *b = sm + blk * F::BB;          // 2-byte aligned
-            const uint32_t d16 = lds_u16(b);
-            const uint32_t w0 = lds_u32_a2(b + 2 + 8 * c), w1 = lds_u32_a2(b + 6 + 8 * c);
-            store8(out, (b0 + blk) * F::QK + 8 * c, K, ldo, q80_eight(d16, w0, w1));
+        // Lane pair j owns block j of the group; lane h takes quants 8h +
+        // {0..7} and 16 + 8h + {0..7}.
+        const int h = lane & 1;
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+            const int blk = (warp * kPasses + ps) * F::BPG + (lane >> 1);
+            if (blk < nb) {
+                const int bo = blk * F::BB;             // 2-byte aligned
+                const uint32_t d16 = lds_u16(sm, bo);
+                const uint2 w0 = lds8_a2(sm, bo + 2 + 8 * h), w1 = lds8_a2(sm, bo + 18 + 8 * h);
+                const uint32_t bi = static_cast<uint32_t>(b0 + blk);
+                stg_v4(dest<F::QK>(out, bi, 8 * h, mode, K, ldo, br), q80_eight(d16, w0.x, w0.y));
+                stg_v4(dest<F::QK>(out, bi, 16 + 8 * h, mode, K, ldo, br), q80_eight(d16, w1.x, w1.y));
+            }
         }
     }
 }
@@ -135,11 +211,21 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *__restrict_
 template <int T>
 cudaError_t launch_t(const void *q, int64_t nblocks, __half *out, int64_t K, int64_t ldo, cudaStream_t s)
 {
-    const int64_t grid = (nblocks + Fmt<T>::G - 1) / Fmt<T>::G;
-    if (grid > 0x7FFFFFFF)
+    using F = Fmt<T>;
+    if (nblocks > 0x7FFFFFFF)   // block indices are 32-bit in the kernel
         return cudaErrorInvalidValue;
+    const int64_t grid = (nblocks + F::G - 1) / F::G;
+    BlockRows br{1u, 0xFFFFFFFFu};
+    int mode = 2;
+    if (ldo == K) {
+        mode = 0;
+    } else if (K % F::QK == 0) {
+        mode = 1;
+        br.bpr = static_cast<uint32_t>(K / F::QK);
+        br.m = 0xFFFFFFFFu / br.bpr;
+    }
     k_dequant<T><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(static_cast<const uint8_t *>(q), nblocks, out,
-                                                                  K, ldo);
+                                                                  K, ldo, mode, br);
     note_launch();
     return cudaGetLastError();
 }

@@ -48,6 +48,7 @@
 #include "mq_decode.cuh"
 #include "mq_internal.h"
 #include "mq_ptx.cuh"
+#include "mq_smem.cuh"
 #include "mq_tile.cuh"
 
 namespace mq {
@@ -100,42 +101,6 @@ __device__ __forceinline__ RowSpan row_span(int64_t n, int64_t K, int64_t kc0, i
     r.s0 = b0 & ~static_cast<int64_t>(15);
     r.bytes = static_cast<uint32_t>(((b1 + 15) & ~static_cast<int64_t>(15)) - r.s0);
     return r;
-}
-
-__device__ __forceinline__ uint32_t lds_u32(uint32_t saddr)
-{
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t lds_u16(uint32_t saddr)
-{
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(saddr));
-    return v;
-}
-
-__device__ __forceinline__ int lds_s8(uint32_t saddr)
-{
-    short v;
-    asm volatile("ld.shared.s8 %0, [%1];" : "=h"(v) : "r"(saddr));
-    return v;
-}
-
-// 32 bytes starting at a 2-byte-aligned shared address, as 8 little-endian
-// words: nine aligned word loads and a funnel shift by 0 or 16 bits.
-__device__ __forceinline__ void lds_32B_a2(uint32_t saddr, uint32_t (&w)[8])
-{
-    const uint32_t base = saddr & ~3u;
-    const uint32_t sh = (saddr & 3u) * 8u;
-    uint32_t t[9];
-#pragma unroll
-    for (int i = 0; i < 9; ++i)
-        t[i] = lds_u32(base + 4 * i);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        w[i] = __funnelshift_r(t[i], t[i + 1], sh);
 }
 
 // Decode 32 consecutive elements starting at element o of the block at

@@ -125,6 +125,17 @@ __device__ __forceinline__ uint4 q4k_eight(float A, float B, uint32_t w0, uint32
                       cvt_f16x2(fma_f32x2(a2, add_f32x2(magic_pair(v1, 2), m2), nb2)));
 }
 
+// Core of the Q6_K decode: v0, v1 hold the eight unsigned 6-bit values
+// (value + 32 of the block definition) one per byte.
+__device__ __forceinline__ uint4 q6k_core(float A, uint32_t v0, uint32_t v1)
+{
+    const uint64_t a2 = f32x2(A, A), m2 = f32x2(-8388640.0f, -8388640.0f);   // -(2^23 + 32)
+    return make_uint4(cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v0, 0), m2))),
+                      cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v0, 2), m2))),
+                      cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v1, 0), m2))),
+                      cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v1, 2), m2))));
+}
+
 // Eight Q6_K outputs: low 4 bits from the nibbles of ql bytes (l0 = bytes
 // 0..3, l1 = 4..7; shift lsh 0 or 4), high 2 bits from bits hsh..hsh+1 of
 // qh bytes (h0, h1).  q6 = value - 32, y = RN16(A * q6) with A = d*sc.
@@ -133,11 +144,16 @@ __device__ __forceinline__ uint4 q6k_eight(float A, uint32_t l0, uint32_t l1, in
 {
     const uint32_t v0 = ((l0 >> lsh) & 0x0F0F0F0Fu) | (((h0 >> hsh) & 0x03030303u) << 4);
     const uint32_t v1 = ((l1 >> lsh) & 0x0F0F0F0Fu) | (((h1 >> hsh) & 0x03030303u) << 4);
-    const uint64_t a2 = f32x2(A, A), m2 = f32x2(-8388640.0f, -8388640.0f);   // -(2^23 + 32)
-    return make_uint4(cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v0, 0), m2))),
-                      cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v0, 2), m2))),
-                      cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v1, 0), m2))),
-                      cvt_f16x2(mul_f32x2(a2, add_f32x2(magic_pair(v1, 2), m2))));
+    return q6k_core(A, v0, v1);
+}
+
+// The 6-bit values of q6k_eight with shift amounts that vary per thread:
+// lsh = 0 or 4 as there; hrot = (hsh + 28) & 31 rotates bits hsh, hsh+1 of
+// every qh byte onto bits 4, 5 of the same byte (a rotation by 28 is a left
+// shift by 4; bits that wrap around land outside the 0x30 mask).
+__device__ __forceinline__ uint32_t q6k_bytes(uint32_t l, int lsh, uint32_t h, int hrot)
+{
+    return ((l >> lsh) & 0x0F0F0F0Fu) | (__funnelshift_r(h, h, hrot) & 0x30303030u);
 }
 
 // Eight Q8_0 outputs from 8 int8 quants (w0 bytes 0..3, w1 bytes 4..7) and

@@ -123,7 +123,7 @@ WORKLOADS = {
     "llama3.1-8b_layer": (LLAMA31_8B, [512]),
     "q8_0_pair": (Q8_0_PAIR, [128, 1024]),
     "small_m_sweep": ([w for w in QWEN25_7B if w[0] in ("gate", "up", "down")],
-                      [1, 8, 32, 128, 512, 2048]),
+                      [1, 8, 32, 128, 256, 512, 2048]),
 }
 
 
