@@ -30,18 +30,24 @@
 //               bulk copy per row of the 16-byte-aligned byte range.  Q6_K
 //               (210 B) and Q8_0 (34 B) blocks are only 2-byte aligned; in
 //               both cases every global access stays 16-byte aligned.
-//   warp 1      TMEM allocation and the MMA issuer (one thread): per raw
-//               chunk one wait for its A stage and X stage, then sixteen
-//               unrolled M=128 x N=BN x K=16 MMAs with A in TMEM.  This
-//               thread shares its SM sub-partition with decode warps, so it
-//               spends as few instructions per MMA as possible.
+//   warps 1, 3  MMA issuers (one thread each; warp 1 also owns the TMEM
+//               allocation): per chunk one wait, sixteen M=128 x N=BN x K=16
+//               MMAs with A in TMEM, one commit.  Two issuers on different
+//               sub-partitions take alternate chunks into separate partial
+//               accumulators (BN <= 64): the issue of an MMA is a short chain
+//               of dependent instructions competing with the decode warps
+//               for issue slots, and one thread alone leaves the tensor pipe
+//               idle between MMAs.
 //   warp 2      activation producer (TMA): the BN x 256 activations of a
-//               chunk (four 64-wide boxes) per stage, up to x_stages ahead.
-//   warps 4-7   epilogue (TMEM -> Y / split-K workspace).
-//   warps 8-15  decoders: thread (row, half) turns 32 raw elements of one
-//               weight row per K step into 16 packed f16 words and stores
-//               them with tcgen05.st into its row's TMEM lane; one barrier
-//               round trip per 256-element chunk.
+//               chunk (four 64-wide boxes) into the chunk slot's X stage.
+//   warps 4-7   epilogue (TMEM -> Y / split-K workspace; sums the partial
+//               accumulators in a fixed order).
+//   warps 8-15  decoders: thread (row, pair of K steps) turns 128 raw
+//               elements of one weight row per chunk into f16 and stores them
+//               with tcgen05.st into its row's TMEM lane.
+// Chunk slots: A stage s (TMEM) and X stage s (shared memory) form one slot;
+// `ready[s]` completes when the decoders have written A and the activations
+// have landed, `done[s]` (an MMA commit) frees both.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -58,15 +64,37 @@ constexpr int kThreadsF = 512;
 constexpr int kDecodeWarp0 = 8;
 constexpr int kDecodeWarps = 8;
 constexpr int kChunkSteps = 4;               // K steps (of 64) per raw stage: 256 K elements
-constexpr int kMaxX = 4, kMaxRaw = 4;
-// TMEM: accumulators in columns [0, 256), two A stages of 128 columns (one
-// raw chunk of 256 K elements, two f16 per column) in [256, 512).
+constexpr int kMaxRaw = 4, kMaxStages = 3;
+// MMA issuers: two (warps 1 and 3, on different SM sub-partitions) taking
+// alternate chunks into separate partial accumulators while BN <= 64, one
+// at BN = 128.  An issuing thread shares its sub-partition's issue slots
+// with the decode warps, and the issue of one tcgen05.mma is a short chain
+// of dependent instructions, so one thread alone cannot keep the tensor pipe
+// busy while the decoders run.
+//
+// TMEM: two accumulator slots (double buffering across units) of
+// kIssuers partial accumulators of BN columns each, then the A stages of
+// 128 columns each (one raw chunk of 256 K elements, two f16 per column):
+// three stages from column 128 for BN <= 32, two from column 256 above.
 constexpr int kTmemCols = 512;
-constexpr uint32_t kACol0 = 256;
-constexpr int kAStages = 2;
 constexpr int kAStageCols = 128;
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kBarBytes = 512;
+
+__host__ __device__ constexpr int issuers_for(int bn)
+{
+    return bn <= 64 ? 2 : 1;
+}
+
+__host__ __device__ constexpr int a_stages_for(int bn)
+{
+    return bn <= 32 ? 3 : 2;
+}
+
+__host__ __device__ constexpr uint32_t a_col0_for(int bn)
+{
+    return bn <= 32 ? 128u : 256u;
+}
 
 template <int QT> struct QF;
 template <> struct QF<8> { static constexpr int QK = 32, BB = 34; };
@@ -160,94 +188,118 @@ __device__ __forceinline__ void decode32<8>(uint32_t b, int o, uint4 (&out)[4])
 // Block-aligned weights (K % 256 == 0): one raw chunk of a row is 256
 // consecutive elements starting on a block boundary -- one Q4_K or Q6_K
 // block, or eight Q8_0 blocks -- at `b` (the row's slot plus its leading
-// misalignment).  These decode the thread's 4 x 32 elements of the chunk
-// (K step st covers elements 64*st + 32*half .. +31) fully unrolled and store
-// each group of 32 into TMEM columns col + 32*st .. +15.  Rows past the
-// weight's end (valid == false) store zeros.  tcgen05.st is .sync.aligned:
-// every lane of the warp must reach the same store, so the stores sit
-// outside any lane-dependent branch.
+// misalignment).  decode_step decodes the 64 elements of K step j of the
+// chunk (j = 0..3; elements 64j + 32h .. +31 for halves h = 0, 1) and stores
+// each half into TMEM columns col + 16h .. +15 (two f16 per column).
+// tcgen05.st is .sync.aligned: j is the same for all lanes of a warp and the
+// stores sit outside any lane-dependent branch.  Rows past the weight's end
+// decode whatever their slot holds: the MMA keeps weight rows apart (row r
+// of A only feeds row r of the accumulator) and the epilogue never stores
+// rows past N, so those values cannot reach Y.
 
-__device__ __forceinline__ void store_step(uint32_t taddr, uint4 (&out)[4], bool valid)
+// int8 held in the low byte of v -> exact f32 (sign flipped to a 0..255
+// bias, 2^23 trick, bias removed).
+__device__ __forceinline__ float s8_to_f32(uint32_t v)
 {
-    if (!valid) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            out[j] = make_uint4(0, 0, 0, 0);
-    }
-    __syncwarp();
-    tmem_st_32x32b_x16(taddr, out);
+    return __int_as_float(0x4B000000u | ((v ^ 0x80u) & 0xFFu)) - 8388736.0f;   // 2^23 + 128
 }
 
 template <int QT>
-__device__ __forceinline__ void decode_chunk(uint32_t b, int half, uint32_t col, bool valid);
+__device__ __forceinline__ void decode_step(uint32_t b, int j, uint32_t col);
 
 template <>
-__device__ __forceinline__ void decode_chunk<12>(uint32_t b, int half, uint32_t col, bool valid)
+__device__ __forceinline__ void decode_step<12>(uint32_t b, int j, uint32_t col)
 {
-    // Q4_K, b 16-byte aligned.  Step st is group p = st: sub-block 2*st+half,
-    // nibbles (low for half 0, high for half 1) of qs bytes 32*st .. +31.
-    const uint4 hdr = lds_v4(b);
+    // Q4_K, b 16-byte aligned.  Step j is group p = j: qs bytes 32j .. +31,
+    // low nibbles for sub-block 2j (half 0), high nibbles for 2j+1 (half 1).
+    const uint4 hdr = lds_v4(b);   // d | dmin, scale bytes 0..3, 4..7, 8..11
+    const uint4 q0 = lds_v4(b + 16 + 32 * j), q1 = lds_v4(b + 32 + 32 * j);
+    // 6-bit scales (scw) and mins (mnw) of sub-blocks 4*(j/2) .. +3, one per
+    // byte: the block format's packing rule applied four bytes at a time.
+    uint32_t scw, mnw;
+    if (j < 2) {
+        scw = hdr.y & 0x3F3F3F3Fu;
+        mnw = hdr.z & 0x3F3F3F3Fu;
+    } else {
+        scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+        mnw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    }
+    const int bsel = 2 * (j & 1);   // bytes of sub-blocks 2j, 2j+1
+    const uint64_t m2 = f32x2(-8388608.0f, -8388608.0f);
     const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
-    const int sh = 4 * half;
-#pragma unroll
-    for (int st = 0; st < 4; ++st) {
-        int sc, m;
-        q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * st + half, sc, m);
-        const float A = __fmul_rn(d, static_cast<float>(sc)), B = __fmul_rn(dmin, static_cast<float>(m));
-        const uint4 q0 = lds_v4(b + 16 + 32 * st), q1 = lds_v4(b + 32 + 32 * st);
+    float A0, A1, nB0, nB1;   // d*sc and -(dmin*m) of the two sub-blocks, exact
+    unpack_f32x2(mul_f32x2(add_f32x2(magic_pair(scw, bsel), m2), f32x2(d, d)), A0, A1);
+    unpack_f32x2(mul_f32x2(add_f32x2(magic_pair(mnw, bsel), m2), f32x2(-dmin, -dmin)), nB0, nB1);
+    {
+        const uint64_t a2 = f32x2(A0, A0), nb2 = f32x2(nB0, nB0);
         uint4 out[4];
-        out[0] = q4k_eight(A, B, q0.x, q0.y, sh);
-        out[1] = q4k_eight(A, B, q0.z, q0.w, sh);
-        out[2] = q4k_eight(A, B, q1.x, q1.y, sh);
-        out[3] = q4k_eight(A, B, q1.z, q1.w, sh);
-        store_step(col + 32 * st, out, valid);
+        out[0] = fma_bytes_eight(a2, nb2, q0.x & 0x0F0F0F0Fu, q0.y & 0x0F0F0F0Fu);
+        out[1] = fma_bytes_eight(a2, nb2, q0.z & 0x0F0F0F0Fu, q0.w & 0x0F0F0F0Fu);
+        out[2] = fma_bytes_eight(a2, nb2, q1.x & 0x0F0F0F0Fu, q1.y & 0x0F0F0F0Fu);
+        out[3] = fma_bytes_eight(a2, nb2, q1.z & 0x0F0F0F0Fu, q1.w & 0x0F0F0F0Fu);
+        __syncwarp();
+        tmem_st_32x32b_x16(col, out);
+    }
+    {
+        // High nibbles stay in place (bytes 16q); A/16 is exact (a power-of-two
+        // scaling of a normal f32), so (A/16)*(16q) = A*q as for the low half.
+        const float a16 = A1 * 0.0625f;
+        const uint64_t a2 = f32x2(a16, a16), nb2 = f32x2(nB1, nB1);
+        uint4 out[4];
+        out[0] = fma_bytes_eight(a2, nb2, q0.x & 0xF0F0F0F0u, q0.y & 0xF0F0F0F0u);
+        out[1] = fma_bytes_eight(a2, nb2, q0.z & 0xF0F0F0F0u, q0.w & 0xF0F0F0F0u);
+        out[2] = fma_bytes_eight(a2, nb2, q1.x & 0xF0F0F0F0u, q1.y & 0xF0F0F0F0u);
+        out[3] = fma_bytes_eight(a2, nb2, q1.z & 0xF0F0F0F0u, q1.w & 0xF0F0F0F0u);
+        __syncwarp();
+        tmem_st_32x32b_x16(col + 16, out);
     }
 }
 
 template <>
-__device__ __forceinline__ void decode_chunk<14>(uint32_t b, int half, uint32_t col, bool valid)
+__device__ __forceinline__ void decode_step<14>(uint32_t b, int j, uint32_t col)
 {
-    // Q6_K, b 2-byte aligned.  Step st covers quarter t = (2*st+half) & 3 of
-    // block half hh = st >> 1: low bits from ql bytes 64*hh + 32*half .. +31
-    // (low nibble for even st, high for odd), high bits from qh bytes
-    // 32*hh .. +31 (bits 2t), scales sc[4*st + 2*half], sc[4*st + 2*half + 1].
+    // Q6_K, b 2-byte aligned.  Step j lies in block half hh = j/2; its half h
+    // is quarter t = 2(j%2) + h: low bits from ql bytes 64hh + 32h .. +31
+    // (low nibbles for even j, high for odd), high bits from qh bytes
+    // 128 + 32hh .. +31 (bits 2t, 2t+1), scales sc[4j + 2h] and sc[4j + 2h + 1].
+    const int hh = j >> 1, odd = j & 1;
     const float d = f16_bits_to_f32(lds_u16(b + 208));
-    uint32_t lq[2][8], hq[2][8];
-    lds_32B_a2(b + 32 * half, lq[0]);
-    lds_32B_a2(b + 64 + 32 * half, lq[1]);
-    lds_32B_a2(b + 128, hq[0]);
-    lds_32B_a2(b + 160, hq[1]);
+    uint32_t hq[8];
+    lds_32B_a2(b + 128 + 32 * hh, hq);
+    const uint32_t scw = lds_u16(b + 192 + 4 * j) | (lds_u16(b + 194 + 4 * j) << 16);
 #pragma unroll
-    for (int st = 0; st < 4; ++st) {
-        const int hh = st >> 1, t = (2 * st + half) & 3;
-        const int lsh = (st & 1) ? 4 : 0, hsh = 2 * t;
-        const int si = 4 * st + 2 * half;
-        const float A0 = __fmul_rn(d, static_cast<float>(lds_s8(b + 192 + si)));
-        const float A1 = __fmul_rn(d, static_cast<float>(lds_s8(b + 193 + si)));
+    for (int h = 0; h < 2; ++h) {
+        uint32_t lq[8];
+        lds_32B_a2(b + 64 * hh + 32 * h, lq);
+        const int lsh = 4 * odd, hsh = 2 * (2 * odd + h);
+        const float A0 = __fmul_rn(d, s8_to_f32(scw >> (16 * h)));
+        const float A1 = __fmul_rn(d, s8_to_f32(scw >> (16 * h + 8)));
         uint4 out[4];
-        out[0] = q6k_eight(A0, lq[hh][0], lq[hh][1], lsh, hq[hh][0], hq[hh][1], hsh);
-        out[1] = q6k_eight(A0, lq[hh][2], lq[hh][3], lsh, hq[hh][2], hq[hh][3], hsh);
-        out[2] = q6k_eight(A1, lq[hh][4], lq[hh][5], lsh, hq[hh][4], hq[hh][5], hsh);
-        out[3] = q6k_eight(A1, lq[hh][6], lq[hh][7], lsh, hq[hh][6], hq[hh][7], hsh);
-        store_step(col + 32 * st, out, valid);
+        out[0] = q6k_eight(A0, lq[0], lq[1], lsh, hq[0], hq[1], hsh);
+        out[1] = q6k_eight(A0, lq[2], lq[3], lsh, hq[2], hq[3], hsh);
+        out[2] = q6k_eight(A1, lq[4], lq[5], lsh, hq[4], hq[5], hsh);
+        out[3] = q6k_eight(A1, lq[6], lq[7], lsh, hq[6], hq[7], hsh);
+        __syncwarp();
+        tmem_st_32x32b_x16(col + 16 * h, out);
     }
 }
 
 template <>
-__device__ __forceinline__ void decode_chunk<8>(uint32_t b, int half, uint32_t col, bool valid)
+__device__ __forceinline__ void decode_step<8>(uint32_t b, int j, uint32_t col)
 {
-    // Q8_0: step st is the whole block 2*st + half (34 bytes, 2-byte aligned).
+    // Q8_0: half h of step j is the whole block 2j + h (34 bytes, 2-byte aligned).
 #pragma unroll
-    for (int st = 0; st < 4; ++st) {
-        const uint32_t blk = b + 34 * (2 * st + half);
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t blk = b + 34 * (2 * j + h);
         const uint32_t d16 = lds_u16(blk);
         uint32_t q[8];
         lds_32B_a2(blk + 2, q);
         uint4 out[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            out[j] = q80_eight(d16, q[2 * j], q[2 * j + 1]);
-        store_step(col + 32 * st, out, valid);
+        for (int i = 0; i < 4; ++i)
+            out[i] = q80_eight(d16, q[2 * i], q[2 * i + 1]);
+        __syncwarp();
+        tmem_st_32x32b_x16(col + 16 * h, out);
     }
 }
 
@@ -259,24 +311,28 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     constexpr int kXSub = BN * kBK * 2;               // one 64-wide K step of activations
     constexpr int kXBytes = kChunkSteps * kXSub;      // one X stage: a whole 256-element chunk
     constexpr int kNAcc = 2;                          // accumulators at TMEM columns [0, 2*BN)
+    constexpr int S = a_stages_for(BN);               // A and X stages (one ring of chunk slots)
     static_assert(BN <= 128, "fused tiles stop at 128 tokens");
-    const int SX = a.x_stages, R = a.raw_stages, RS = a.raw_rs;
+    constexpr int kIssuers = issuers_for(BN);
+    constexpr uint32_t kACol0 = a_col0_for(BN);
+    static_assert(kNAcc * kIssuers * BN <= static_cast<int>(kACol0) && kACol0 + S * kAStageCols <= kTmemCols,
+                  "TMEM budget");
+    const int R = a.raw_stages, RS = a.raw_rs;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sX = base;
-    uint8_t *sR = sX + SX * kXBytes;
+    uint8_t *sR = sX + S * kXBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sR + static_cast<size_t>(R) * kTileRows * RS);
-    uint64_t *raw_full = bars;
-    uint64_t *raw_empty = raw_full + kMaxRaw;
-    uint64_t *x_full = raw_empty + kMaxRaw;
-    uint64_t *x_empty = x_full + kMaxX;
-    uint64_t *a_full = x_empty + kMaxX;
-    uint64_t *a_empty = a_full + kAStages;
-    uint64_t *tfull = a_empty + kAStages;
+    uint64_t *raw_full = bars;                // raw chunk landed (TMA bytes)
+    uint64_t *raw_empty = raw_full + kMaxRaw; // raw chunk decoded (decoder warps)
+    uint64_t *x_full = raw_empty + kMaxRaw;   // activation chunk landed (TMA bytes)
+    uint64_t *ready = x_full + kMaxStages;    // A stage decoded and its X stage landed
+    uint64_t *done = ready + kMaxStages;      // MMAs of the chunk slot finished (commit)
+    uint64_t *tfull = done + kMaxStages;
     uint64_t *tempty = tfull + 2;
-    uint64_t *drain = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *drain = tempty + 2;             // one per issuer
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -288,19 +344,17 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             mbar_init(&raw_full[r], 1);
             mbar_init(&raw_empty[r], kDecodeWarps);
         }
-        for (int s = 0; s < SX; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&x_full[s], 1);
-            mbar_init(&x_empty[s], 1);
-        }
-        for (int s = 0; s < kAStages; ++s) {
-            mbar_init(&a_full[s], kDecodeWarps);
-            mbar_init(&a_empty[s], 1);
+            mbar_init(&ready[s], kDecodeWarps);
+            mbar_init(&done[s], 1);
         }
         for (int i = 0; i < kNAcc; ++i) {
-            mbar_init(&tfull[i], 1);
+            mbar_init(&tfull[i], kIssuers);
             mbar_init(&tempty[i], 4);
         }
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -391,12 +445,17 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 if (issued & (1u << i))
                     mbar_wait_bounded(&raw_full[i], (iparity >> i) & 1u, &no_abort, a.status);
         }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer: A from TMEM, B (activations) from shared memory
+    } else if (warp == 1 || warp == 3) {
+        const int t = warp == 1 ? 0 : 1;   // issuer index
+        if (lane == 0 && t < kIssuers) {
+            // ---------------- MMA issuer t: A from TMEM, B (activations) from
+            // shared memory.  Chunk i of a unit (i = 0, 1, ...) belongs to
+            // issuer i % kIssuers and accumulates into that issuer's partial
+            // accumulator; both issuers walk the whole chunk ring to keep
+            // their slot and phase in step.
             constexpr uint32_t idesc = idesc_f16_f32(kTileRows, BN);
-            int sa = 0, sx = 0;
-            uint32_t pa = 0, px = 0;
+            int s = 0;
+            uint32_t ph = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
@@ -404,61 +463,54 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 const UnitInfo ui = unit_info(a, u);
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, a.status))
                     break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
-                for (int kb = ui.kb0; ok && kb < ui.kb1; kb += kChunkSteps) {
-                    const int steps = ui.kb1 - kb < kChunkSteps ? ui.kb1 - kb : kChunkSteps;
-                    if (!mbar_wait_bounded(&a_full[sa], pa, abort_flag, a.status) ||
-                        !mbar_wait_bounded(&x_full[sx], px, abort_flag, a.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(sa * kAStageCols);
-                    const uint64_t b_desc = sdesc_k_sw128(smem_u32(sX + sx * kXBytes));
-                    const uint32_t acc_in = kb > ui.kb0 ? 1u : 0u;
-                    if (steps == kChunkSteps) {
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>((acc * kIssuers + t) * BN);
+                int i = 0;
+                for (int kb = ui.kb0; kb < ui.kb1; kb += kChunkSteps, ++i) {
+                    if (i % kIssuers == t) {
+                        const int steps = ui.kb1 - kb < kChunkSteps ? ui.kb1 - kb : kChunkSteps;
+                        if (!mbar_wait_bounded(&ready[s], ph, abort_flag, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(s * kAStageCols);
+                        const uint64_t b_desc = sdesc_k_sw128(smem_u32(sX + s * kXBytes));
+                        const uint32_t acc_in = i >= kIssuers ? 1u : 0u;
+                        if (steps == kChunkSteps) {
 #pragma unroll
-                        for (int st = 0; st < kChunkSteps; ++st)
-#pragma unroll
-                            for (int k = 0; k < kBK / 16; ++k)
-                                umma_f16_ta(d_tmem, a_tmem + static_cast<uint32_t>(st * 32 + k * 8),
-                                            b_desc + static_cast<uint64_t>((st * kXSub + 32 * k) >> 4), idesc,
-                                            (st > 0 || k > 0) ? 1u : acc_in);
-                    } else {
-                        for (int st = 0; st < steps; ++st)
-#pragma unroll
-                            for (int k = 0; k < kBK / 16; ++k)
-                                umma_f16_ta(d_tmem, a_tmem + static_cast<uint32_t>(st * 32 + k * 8),
-                                            b_desc + static_cast<uint64_t>((st * kXSub + 32 * k) >> 4), idesc,
-                                            (st > 0 || k > 0) ? 1u : acc_in);
+                            for (int k = 0; k < kChunkSteps * (kBK / 16); ++k)
+                                umma_f16_ta(d_tmem, a_tmem + static_cast<uint32_t>(k * 8),
+                                            b_desc + static_cast<uint64_t>(((k >> 2) * kXSub + 32 * (k & 3)) >> 4), idesc,
+                                            k > 0 ? 1u : acc_in);
+                        } else {
+                            for (int k = 0; k < steps * (kBK / 16); ++k)
+                                umma_f16_ta(d_tmem, a_tmem + static_cast<uint32_t>(k * 8),
+                                            b_desc + static_cast<uint64_t>(((k >> 2) * kXSub + 32 * (k & 3)) >> 4), idesc,
+                                            k > 0 ? 1u : acc_in);
+                        }
+                        umma_commit(&done[s]);
                     }
-                    umma_commit(&a_empty[sa]);
-                    umma_commit(&x_empty[sx]);
-                    if (++sa == kAStages) {
-                        sa = 0;
-                        pa ^= 1u;
-                    }
-                    if (++sx == SX) {
-                        sx = 0;
-                        px ^= 1u;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
                     }
                 }
                 if (!ok)
                     break;
-                umma_commit(&tfull[acc]);
+                umma_commit(&tfull[acc]);   // also when this issuer had no chunk in the unit
                 if (++acc == kNAcc) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
-            umma_commit(drain);
+            umma_commit(&drain[t]);
             volatile int no_abort = 0;
-            mbar_wait_bounded(drain, 0, &no_abort, a.status);
+            mbar_wait_bounded(&drain[t], 0, &no_abort, a.status);
         }
     } else if (warp == 2) {
         if (lane == 0) {
-            // ---------------- activation-tile producer
+            // ---------------- activation-tile producer: chunk slot s is free
+            // again once the MMAs that read it are done.
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0, iparity = 0;
@@ -468,7 +520,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 const int m0 = (ui.tile % a.m_tiles) * BN;
                 for (int kb = ui.kb0; kb < ui.kb1; kb += kChunkSteps) {
                     const int steps = ui.kb1 - kb < kChunkSteps ? ui.kb1 - kb : kChunkSteps;
-                    if (!mbar_wait_bounded(&x_empty[s], ph ^ 1u, abort_flag, a.status)) {
+                    if (!mbar_wait_bounded(&done[s], ph ^ 1u, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
@@ -477,7 +529,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                         tma_load_2d(sX + s * kXBytes + st * kXSub, &tm_x, &x_full[s], (kb + st) * kBK, m0);
                     issued |= 1u << s;
                     iparity = (iparity & ~(1u << s)) | (ph << s);
-                    if (++s == SX) {
+                    if (++s == S) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -485,83 +537,106 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             }
             if (!ok) {
                 volatile int no_abort = 0;
-                for (int i = 0; i < SX; ++i)
+                for (int i = 0; i < S; ++i)
                     if (issued & (1u << i))
                         mbar_wait_bounded(&x_full[i], (iparity >> i) & 1u, &no_abort, a.status);
             }
         }
     } else if (warp >= 4 && warp < 8) {
         // ---------------- epilogue: warps 4..7 own TMEM lane quarters 0..3
-        epilogue_role<BN, kNAcc>(a, tmem, tfull, tempty, abort_flag, warp, lane);
+        epilogue_role<BN, kNAcc, kIssuers>(a, tmem, tfull, tempty, abort_flag, warp, lane, kChunkSteps);
     } else if (warp >= kDecodeWarp0) {
-        // ---------------- decoders: thread (row, half) writes, for each 64-wide
-        // K step of a raw chunk, 32 f16 of its row into TMEM lane `row`,
-        // columns (step*32 + half*16) .. +15 of the chunk's A stage.  Warp w
-        // holds rows 32*(w%4) .. +31, the TMEM lanes it may access.
-        const int dt = threadIdx.x - kDecodeWarp0 * 32;
-        const int row = dt & (kTileRows - 1);
-        const int half = dt >> 7;
+        // ---------------- decoders: warp w holds weight rows 32*(w%4) .. +31
+        // (the TMEM lanes it may access) and K steps j0 = 2*((w-8)/4) and
+        // j0+1 of every chunk: thread (row, j0) writes the 128 f16 of its
+        // row for those steps into TMEM lane `row`, columns 32*j0 .. +63 of
+        // the chunk's A stage.  The first decoder warp also waits for the
+        // chunk's activations before it arrives, so `ready` means "A decoded
+        // and X landed".
+        const int dw = warp - kDecodeWarp0;
+        const int row = (warp & 3) * 32 + lane;
+        const int j0 = 2 * (dw >> 2);
         const uint32_t lane_base = static_cast<uint32_t>(row & ~31) << 16;
         // shared-memory row of this weight row inside a raw stage
         const int srow = TMA_RAW ? (row % g) * rows_per_class + row / g : row;
-        int r = 0, sa = 0;
-        uint32_t rph = 0, pa = 0;
+        const uint32_t raw_row0 = smem_u32(sR) + static_cast<uint32_t>(srow * RS);
+        const uint32_t slot_bytes = static_cast<uint32_t>(kTileRows * RS);
+        const uint32_t a_col0 = tmem + lane_base + kACol0 + static_cast<uint32_t>(32 * j0);
+        // bytes of one 256-element chunk inside a row (K % 256 == 0)
+        constexpr uint32_t kChunkRowBytes = kChunkSteps * kBK / F::QK * F::BB;
+        int r = 0, s = 0;
+        uint32_t rph = 0, ph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
             const UnitInfo ui = unit_info(a, u);
             const int64_t n = static_cast<int64_t>(ui.tile / a.m_tiles) * kTileRows + row;
             const bool valid = n < a.N;
+            // Tensor-map path: the slot row of a chunk starts at the 16-byte
+            // boundary at or below the chunk's first byte, so the chunk sits
+            // lead = (mis + ob) % 16 bytes into it, where mis is the row's
+            // misalignment in its class map and ob the chunk's offset in the
+            // row.  Rows past N read their zero-filled slot.
+            uint32_t mis = 0, ob = 0;
+            if (TMA_RAW) {
+                mis = valid ? static_cast<uint32_t>(((n % g) * a.raw_rb) & 15) : 0u;
+                ob = static_cast<uint32_t>(ui.kb0 / kChunkSteps) * kChunkRowBytes;
+            }
             for (int kb = ui.kb0; ok && kb < ui.kb1; kb += kChunkSteps) {
                 const int steps = ui.kb1 - kb < kChunkSteps ? ui.kb1 - kb : kChunkSteps;
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&raw_full[r], rph, abort_flag, a.status) &&
-                                                 mbar_wait_bounded(&a_empty[sa], pa ^ 1u, abort_flag, a.status))) {
+                                                 mbar_wait_bounded(&done[s], ph ^ 1u, abort_flag, a.status))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // Byte position in the stream that shared-memory byte 0 of
-                // this row's raw slot holds.
-                int64_t s0 = 0;
-                if (TMA_RAW) {
-                    const int64_t ob = static_cast<int64_t>(kb) * kBK / F::QK * F::BB;
-                    const int64_t mis = ((n % g) * a.raw_rb) & 15;
-                    s0 = n * a.raw_rb - mis + ((mis + ob) & ~static_cast<int64_t>(15));
-                } else if (valid) {
-                    s0 = row_span<QT>(n, a.K, static_cast<int64_t>(kb) * kBK, static_cast<int64_t>(steps) * kBK).s0;
-                }
-                const uint32_t raw_row =
-                    smem_u32(sR + static_cast<size_t>(r) * kTileRows * RS + static_cast<size_t>(srow) * RS);
-                const uint32_t a_col = tmem + lane_base + kACol0 + static_cast<uint32_t>(sa * kAStageCols + half * 16);
+                const uint32_t raw_row = raw_row0 + static_cast<uint32_t>(r) * slot_bytes;
+                const uint32_t a_col = a_col0 + static_cast<uint32_t>(s * kAStageCols);
                 if (TMA_RAW && steps == kChunkSteps) {
-                    // The chunk's first block sits (mis + ob) % 16 bytes into
-                    // the slot.  Rows past N read their (zero-filled) slot and
-                    // store zeros.
-                    const uint32_t lead = valid ? static_cast<uint32_t>(n * a.raw_rb +
-                                                                        static_cast<int64_t>(kb) * kBK / F::QK * F::BB - s0)
-                                                : 0u;
-                    decode_chunk<QT>(raw_row + lead, half, a_col, valid);
-                } else for (int st = 0; st < steps; ++st) {
-                    uint4 out[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                                    make_uint4(0, 0, 0, 0)};
-                    if (valid) {
-                        const int64_t es = n * a.K + static_cast<int64_t>(kb + st) * kBK + 32 * half;
-                        const int64_t blk = es / F::QK;
-                        const int o = static_cast<int>(es - blk * F::QK);
-                        decode32<QT>(raw_row + static_cast<uint32_t>(blk * F::BB - s0), o, out);
+                    const uint32_t blk = raw_row + ((mis + ob) & 15u);
+                    decode_step<QT>(blk, j0, a_col);
+                    decode_step<QT>(blk, j0 + 1, a_col + 32);
+                    ob += kChunkRowBytes;
+                } else {
+                    // Bulk-copy path: the slot row holds the stream from the
+                    // 16-byte boundary at or below the chunk's first block.
+                    const int64_t s0 =
+                        valid ? row_span<QT>(n, a.K, static_cast<int64_t>(kb) * kBK, static_cast<int64_t>(steps) * kBK).s0
+                              : 0;
+#pragma unroll 1
+                    for (int j = j0; j < j0 + 2 && j < steps; ++j) {
+#pragma unroll 1
+                        for (int h = 0; h < 2; ++h) {
+                            uint4 out[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                                            make_uint4(0, 0, 0, 0)};
+                            if (valid) {
+                                const int64_t es = n * a.K + static_cast<int64_t>(kb + j) * kBK + 32 * h;
+                                const int64_t blk = es / F::QK;
+                                const int o = static_cast<int>(es - blk * F::QK);
+                                decode32<QT>(raw_row + static_cast<uint32_t>(blk * F::BB - s0), o, out);
+                            }
+                            __syncwarp();
+                            tmem_st_32x32b_x16(a_col + static_cast<uint32_t>(32 * (j - j0) + 16 * h), out);
+                        }
                     }
-                    __syncwarp();
-                    tmem_st_32x32b_x16(a_col + static_cast<uint32_t>(st * 32), out);
                 }
                 tmem_st_wait();
                 tc_fence_before();
+                bool xok = true;
+                if (dw == 0 && lane == 0)
+                    xok = mbar_wait_bounded(&x_full[s], ph, abort_flag, a.status);
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&a_full[sa]);
                     mbar_arrive(&raw_empty[r]);
+                    if (xok)
+                        mbar_arrive(&ready[s]);
                 }
-                if (++sa == kAStages) {
-                    sa = 0;
-                    pa ^= 1u;
+                if (!__shfl_sync(0xFFFFFFFFu, xok, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
                 }
                 if (++r == R) {
                     r = 0;
@@ -586,10 +661,10 @@ struct FusedLayout {
 int qk_of(int qt) { return qt == 8 ? 32 : 256; }
 int bb_of(int qt) { return qt == 8 ? 34 : (qt == 12 ? 144 : 210); }
 
-// Shared-memory plan: per-row raw slot size and the depth of the raw and
-// activation rings within 227 KB (the f16 weight operand lives in TMEM).
-// Preferred depths: raw 4 chunks (1024 K elements ahead), activations
-// 4/4/3/2 chunks for BN = 16/32/64/128; the larger ring gives way first.
+// Shared-memory plan: per-row raw slot size and the depth of the raw ring
+// within 227 KB (the f16 weight operand lives in TMEM; the activation ring
+// has one slot per A stage).  Preferred raw depth: 4 chunks (1024 K elements
+// ahead), reduced while the plan does not fit.
 FusedLayout fused_layout(int qt, int bn, bool tma_raw)
 {
     FusedLayout L{};
@@ -606,22 +681,14 @@ FusedLayout fused_layout(int qt, int bn, bool tma_raw)
     const int xb = kChunkSteps * bn * kBK * 2;   // one chunk of activations
     const int raw = kTileRows * L.rs;
     const int budget = kSmemLimit - 1024 - kBarBytes;
-    L.x_stages = bn <= 32 ? 4 : (bn <= 64 ? 3 : 2);
+    L.x_stages = a_stages_for(bn);
     L.raw_stages = kMaxRaw;
-    auto total = [&] { return L.x_stages * xb + L.raw_stages * raw; };
-    while (total() > budget) {
-        if (L.raw_stages > 2 && L.raw_stages * raw >= L.x_stages * xb)
-            --L.raw_stages;
-        else if (L.x_stages > 2)
-            --L.x_stages;
-        else if (L.raw_stages > 2)
-            --L.raw_stages;
-        else if (L.x_stages > 1)
-            --L.x_stages;   // wide raw slots (rows starting inside blocks) at BN = 128
-        else
+    while (L.x_stages * xb + L.raw_stages * raw > budget) {
+        if (L.raw_stages == 1)
             return FusedLayout{};
+        --L.raw_stages;   // one stage only for wide raw slots (rows starting inside blocks) at BN = 128
     }
-    L.smem = 1024 + total() + kBarBytes;
+    L.smem = 1024 + L.x_stages * xb + L.raw_stages * raw + kBarBytes;
     return L;
 }
 
@@ -634,7 +701,7 @@ cudaError_t launch_f(const CUtensorMap &tx, const RawMaps &maps, const GemmArgs 
         return cudaErrorInvalidConfiguration;
     GemmArgs a = a0;
     a.raw_rs = L.rs;
-    a.a_stages = kAStages;
+    a.a_stages = L.x_stages;
     a.x_stages = L.x_stages;
     a.raw_stages = L.raw_stages;
     static bool attr_done[64] = {};

@@ -101,6 +101,11 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
     return d;
 }
 
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
 // Two f32 lanes -> f16x2 (lane 0 in the low half), round to nearest even.
 __device__ __forceinline__ uint32_t cvt_f16x2(uint64_t v)
 {
@@ -109,6 +114,20 @@ __device__ __forceinline__ uint32_t cvt_f16x2(uint64_t v)
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Eight outputs y_j = RN16(RN32(a * c_j - b)) where c_j is byte j of (v0, v1)
+// (bytes 0..3 of v0 first), given a2 = {a, a} and nb2 = {-b, -b}: the byte
+// permute puts c_j under the exponent of 2^23, 2^23 is subtracted exactly,
+// then one packed FMA and one packed f32 -> f16 conversion per two outputs.
+// Exact whenever a * c_j is exact in f32.
+__device__ __forceinline__ uint4 fma_bytes_eight(uint64_t a2, uint64_t nb2, uint32_t v0, uint32_t v1)
+{
+    const uint64_t m2 = f32x2(-8388608.0f, -8388608.0f);
+    return make_uint4(cvt_f16x2(fma_f32x2(a2, add_f32x2(magic_pair(v0, 0), m2), nb2)),
+                      cvt_f16x2(fma_f32x2(a2, add_f32x2(magic_pair(v0, 2), m2), nb2)),
+                      cvt_f16x2(fma_f32x2(a2, add_f32x2(magic_pair(v1, 0), m2), nb2)),
+                      cvt_f16x2(fma_f32x2(a2, add_f32x2(magic_pair(v1, 2), m2), nb2)));
 }
 
 // Eight Q4_K outputs of one sub-block: nibbles taken from the 8 bytes held in

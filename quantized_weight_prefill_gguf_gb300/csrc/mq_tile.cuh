@@ -51,11 +51,16 @@ __device__ __forceinline__ UnitInfo unit_info(const GemmArgs &a, int u)
 // reads it 32 columns (tokens) at a time and stores: Y[m, n] for a whole
 // tile, the partial plane ws[slot][part][col][row] for a split unit.  In
 // both cases the 32 lanes of a store instruction write 32 consecutive
-// floats.  Then it hands the accumulator back to the MMA warp.  NACC
-// accumulators of BN columns each sit at TMEM columns 0, BN, ...
-template <int BN, int NACC = 2>
+// floats.  Then it hands the accumulator back to the MMA warp.
+//
+// TMEM layout: NACC accumulator slots (double buffering across units), each
+// made of NPART partial accumulators of BN columns, slot a part p at column
+// (a*NPART + p)*BN.  Partial accumulators come from MMA issuers that take
+// alternate K chunks of the unit; a unit of c chunks has min(c, NPART) of
+// them, and their sum is formed here in part order (0 + 1).
+template <int BN, int NACC = 2, int NPART = 1>
 __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, uint64_t *tfull, uint64_t *tempty,
-                                              volatile int *abort_flag, int warp, int lane)
+                                              volatile int *abort_flag, int warp, int lane, int kb_chunk = 1)
 {
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -69,16 +74,34 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
         tc_fence_after();
         const int64_t n = static_cast<int64_t>(ui.tile / a.m_tiles) * kTileRows + row;
         const int64_t m0 = static_cast<int64_t>(ui.tile % a.m_tiles) * BN;
+        const int nchunks = (ui.kb1 - ui.kb0 + kb_chunk - 1) / kb_chunk;
+        const bool two = NPART == 2 && nchunks >= 2;
         constexpr int kCols = BN < 32 ? BN : 32;   // columns per TMEM load
 #pragma unroll 1
         for (int c = 0; c < BN; c += kCols) {
             uint32_t r[32];
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + c);
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * NPART * BN + c);
             if constexpr (kCols == 32) {
                 tmem_ld_32x32b_x32(taddr, r);
             } else {
                 uint32_t (&r16)[16] = *reinterpret_cast<uint32_t (*)[16]>(r);
                 tmem_ld_32x32b_x16(taddr, r16);
+            }
+            if constexpr (NPART == 2) {
+                if (two) {
+                    uint32_t r2[32];
+                    if constexpr (kCols == 32) {
+                        tmem_ld_32x32b_x32(taddr + BN, r2);
+                    } else {
+                        uint32_t (&r16)[16] = *reinterpret_cast<uint32_t (*)[16]>(r2);
+                        tmem_ld_32x32b_x16(taddr + BN, r16);
+                    }
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < kCols; ++j)
+                        r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), __uint_as_float(r2[j])));
+                }
             }
             tmem_ld_wait();
             if (ui.part < 0) {
