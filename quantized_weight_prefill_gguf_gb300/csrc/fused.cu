@@ -31,20 +31,23 @@
 //               (210 B) and Q8_0 (34 B) blocks are only 2-byte aligned; in
 //               both cases every global access stays 16-byte aligned.
 //   warps 1, 3  MMA issuers (one thread each; warp 1 also owns the TMEM
-//               allocation): per chunk one wait, sixteen M=128 x N=BN x K=16
-//               MMAs with A in TMEM, one commit.  Two issuers on different
-//               sub-partitions take alternate chunks into separate partial
-//               accumulators (BN <= 64): the issue of an MMA is a short chain
-//               of dependent instructions competing with the decode warps
-//               for issue slots, and one thread alone leaves the tensor pipe
-//               idle between MMAs.
+//               allocation): per chunk one wait, M=128 x N=BN x K=16 MMAs
+//               with A in TMEM, one commit.  With two issuers (BN <= 64),
+//               on different sub-partitions, each takes two of the chunk's
+//               four K steps into its own partial accumulator: the issue of
+//               an MMA is a short chain of dependent instructions competing
+//               with the decode warps for issue slots, and one thread alone
+//               leaves the tensor pipe idle between MMAs.
 //   warp 2      activation producer (TMA): the BN x 256 activations of a
 //               chunk (four 64-wide boxes) into the chunk slot's X stage.
 //   warps 4-7   epilogue (TMEM -> Y / split-K workspace; sums the partial
 //               accumulators in a fixed order).
 //   warps 8-15  decoders: thread (row, pair of K steps) turns 128 raw
 //               elements of one weight row per chunk into f16 and stores them
-//               with tcgen05.st into its row's TMEM lane.
+//               with tcgen05.st into its row's TMEM lane.  Eight warps keep
+//               the integer pipe busy; more of them take issue slots from
+//               the MMA issuers (measured: ~86 cycles per MMA next to 8 busy
+//               warps, ~220 next to 30).
 // Chunk slots: A stage s (TMEM) and X stage s (shared memory) form one slot;
 // `ready[s]` completes when the decoders have written A and the activations
 // have landed, `done[s]` (an MMA commit) frees both.
@@ -60,14 +63,15 @@
 namespace mq {
 namespace {
 
-constexpr int kThreadsF = 512;
 constexpr int kDecodeWarp0 = 8;
-constexpr int kDecodeWarps = 8;
+constexpr int kDecodeWarps = 8;                         // 8 or 16
+constexpr int kThreadsF = (kDecodeWarp0 + kDecodeWarps) * 32;
+constexpr int kStepsPerThread = 16 / kDecodeWarps;      // K steps of a chunk per decoder thread
 constexpr int kChunkSteps = 4;               // K steps (of 64) per raw stage: 256 K elements
-constexpr int kMaxRaw = 4, kMaxStages = 3;
-// MMA issuers: two (warps 1 and 3, on different SM sub-partitions) taking
-// alternate chunks into separate partial accumulators while BN <= 64, one
-// at BN = 128.  An issuing thread shares its sub-partition's issue slots
+constexpr int kMaxRaw = 8, kMaxStages = 3;
+// MMA issuers: two (warps 1 and 3, on different SM sub-partitions) each
+// taking half of every chunk's K steps into its own partial accumulator
+// while BN <= 64, one at BN = 128.  An issuing thread shares its sub-partition's issue slots
 // with the decode warps, and the issue of one tcgen05.mma is a short chain
 // of dependent instructions, so one thread alone cannot keep the tensor pipe
 // busy while the decoders run.
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(&x_full[s], 1);
             mbar_init(&ready[s], kDecodeWarps);
-            mbar_init(&done[s], 1);
+            mbar_init(&done[s], kIssuers);
         }
         for (int i = 0; i < kNAcc; ++i) {
             mbar_init(&tfull[i], kIssuers);
@@ -449,11 +453,12 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         const int t = warp == 1 ? 0 : 1;   // issuer index
         if (lane == 0 && t < kIssuers) {
             // ---------------- MMA issuer t: A from TMEM, B (activations) from
-            // shared memory.  Chunk i of a unit (i = 0, 1, ...) belongs to
-            // issuer i % kIssuers and accumulates into that issuer's partial
-            // accumulator; both issuers walk the whole chunk ring to keep
-            // their slot and phase in step.
+            // shared memory.  Issuer t takes K steps [kSteps*t, kSteps*(t+1))
+            // of every chunk (kSteps = 4 / kIssuers) into its own partial
+            // accumulator and commits `done` once per chunk (the barrier
+            // completes with one commit per issuer).
             constexpr uint32_t idesc = idesc_f16_f32(kTileRows, BN);
+            constexpr int kSteps = kChunkSteps / kIssuers;
             int s = 0;
             uint32_t ph = 0;
             int acc = 0;
@@ -464,32 +469,33 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, a.status))
                     break;
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>((acc * kIssuers + t) * BN);
-                int i = 0;
-                for (int kb = ui.kb0; kb < ui.kb1; kb += kChunkSteps, ++i) {
-                    if (i % kIssuers == t) {
-                        const int steps = ui.kb1 - kb < kChunkSteps ? ui.kb1 - kb : kChunkSteps;
-                        if (!mbar_wait_bounded(&ready[s], ph, abort_flag, a.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(s * kAStageCols);
-                        const uint64_t b_desc = sdesc_k_sw128(smem_u32(sX + s * kXBytes));
-                        const uint32_t acc_in = i >= kIssuers ? 1u : 0u;
-                        if (steps == kChunkSteps) {
-#pragma unroll
-                            for (int k = 0; k < kChunkSteps * (kBK / 16); ++k)
-                                umma_f16_ta(d_tmem, a_tmem + static_cast<uint32_t>(k * 8),
-                                            b_desc + static_cast<uint64_t>(((k >> 2) * kXSub + 32 * (k & 3)) >> 4), idesc,
-                                            k > 0 ? 1u : acc_in);
-                        } else {
-                            for (int k = 0; k < steps * (kBK / 16); ++k)
-                                umma_f16_ta(d_tmem, a_tmem + static_cast<uint32_t>(k * 8),
-                                            b_desc + static_cast<uint64_t>(((k >> 2) * kXSub + 32 * (k & 3)) >> 4), idesc,
-                                            k > 0 ? 1u : acc_in);
-                        }
-                        umma_commit(&done[s]);
+                for (int kb = ui.kb0; kb < ui.kb1; kb += kChunkSteps) {
+                    const int steps = ui.kb1 - kb < kChunkSteps ? ui.kb1 - kb : kChunkSteps;
+                    if (!mbar_wait_bounded(&ready[s], ph, abort_flag, a.status)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(s * kAStageCols);
+                    const uint64_t b_desc = sdesc_k_sw128(smem_u32(sX + s * kXBytes));
+                    const uint32_t acc_in = kb > ui.kb0 ? 1u : 0u;
+                    const int st0 = kSteps * t;
+                    if (steps == kChunkSteps) {
+#pragma unroll
+                        for (int k = 0; k < kSteps * (kBK / 16); ++k) {
+                            const int kk = st0 * (kBK / 16) + k;
+                            umma_f16_ta(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8),
+                                        b_desc + static_cast<uint64_t>(((kk >> 2) * kXSub + 32 * (kk & 3)) >> 4), idesc,
+                                        k > 0 ? 1u : acc_in);
+                        }
+                    } else {
+                        const int st1 = steps < st0 + kSteps ? steps : st0 + kSteps;
+                        for (int kk = st0 * (kBK / 16); kk < st1 * (kBK / 16); ++kk)
+                            umma_f16_ta(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8),
+                                        b_desc + static_cast<uint64_t>(((kk >> 2) * kXSub + 32 * (kk & 3)) >> 4), idesc,
+                                        kk > st0 * (kBK / 16) ? 1u : acc_in);
+                    }
+                    umma_commit(&done[s]);
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
@@ -497,7 +503,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 }
                 if (!ok)
                     break;
-                umma_commit(&tfull[acc]);   // also when this issuer had no chunk in the unit
+                umma_commit(&tfull[acc]);
                 if (++acc == kNAcc) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -544,18 +550,18 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         }
     } else if (warp >= 4 && warp < 8) {
         // ---------------- epilogue: warps 4..7 own TMEM lane quarters 0..3
-        epilogue_role<BN, kNAcc, kIssuers>(a, tmem, tfull, tempty, abort_flag, warp, lane, kChunkSteps);
+        epilogue_role<BN, kNAcc, kIssuers>(a, tmem, tfull, tempty, abort_flag, warp, lane, kChunkSteps / kIssuers);
     } else if (warp >= kDecodeWarp0) {
         // ---------------- decoders: warp w holds weight rows 32*(w%4) .. +31
-        // (the TMEM lanes it may access) and K steps j0 = 2*((w-8)/4) and
-        // j0+1 of every chunk: thread (row, j0) writes the 128 f16 of its
-        // row for those steps into TMEM lane `row`, columns 32*j0 .. +63 of
-        // the chunk's A stage.  The first decoder warp also waits for the
+        // (the TMEM lanes it may access) and kStepsPerThread K steps from
+        // j0 = kStepsPerThread*((w-8)/4) of every chunk: thread (row, j0)
+        // writes the f16 of its row for those steps into TMEM lane `row`,
+        // columns 32*j0 .. of the chunk's A stage.  The first decoder warp also waits for the
         // chunk's activations before it arrives, so `ready` means "A decoded
         // and X landed".
         const int dw = warp - kDecodeWarp0;
         const int row = (warp & 3) * 32 + lane;
-        const int j0 = 2 * (dw >> 2);
+        const int j0 = kStepsPerThread * (dw >> 2);
         const uint32_t lane_base = static_cast<uint32_t>(row & ~31) << 16;
         // shared-memory row of this weight row inside a raw stage
         const int srow = TMA_RAW ? (row % g) * rows_per_class + row / g : row;
@@ -593,8 +599,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 const uint32_t a_col = a_col0 + static_cast<uint32_t>(s * kAStageCols);
                 if (TMA_RAW && steps == kChunkSteps) {
                     const uint32_t blk = raw_row + ((mis + ob) & 15u);
-                    decode_step<QT>(blk, j0, a_col);
-                    decode_step<QT>(blk, j0 + 1, a_col + 32);
+#pragma unroll
+                    for (int jj = 0; jj < kStepsPerThread; ++jj)
+                        decode_step<QT>(blk, j0 + jj, a_col + 32 * jj);
                     ob += kChunkRowBytes;
                 } else {
                     // Bulk-copy path: the slot row holds the stream from the
@@ -603,7 +610,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                         valid ? row_span<QT>(n, a.K, static_cast<int64_t>(kb) * kBK, static_cast<int64_t>(steps) * kBK).s0
                               : 0;
 #pragma unroll 1
-                    for (int j = j0; j < j0 + 2 && j < steps; ++j) {
+                    for (int j = j0; j < j0 + kStepsPerThread && j < steps; ++j) {
 #pragma unroll 1
                         for (int h = 0; h < 2; ++h) {
                             uint4 out[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
@@ -663,8 +670,9 @@ int bb_of(int qt) { return qt == 8 ? 34 : (qt == 12 ? 144 : 210); }
 
 // Shared-memory plan: per-row raw slot size and the depth of the raw ring
 // within 227 KB (the f16 weight operand lives in TMEM; the activation ring
-// has one slot per A stage).  Preferred raw depth: 4 chunks (1024 K elements
-// ahead), reduced while the plan does not fit.
+// has one slot per A stage).  The raw ring takes what is left, up to 8
+// chunks: under load a raw chunk takes ~3 us from issue to arrival, and the
+// chunks in flight per SM set the stream rate.
 FusedLayout fused_layout(int qt, int bn, bool tma_raw)
 {
     FusedLayout L{};

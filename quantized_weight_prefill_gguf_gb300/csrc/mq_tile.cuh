@@ -55,12 +55,13 @@ __device__ __forceinline__ UnitInfo unit_info(const GemmArgs &a, int u)
 //
 // TMEM layout: NACC accumulator slots (double buffering across units), each
 // made of NPART partial accumulators of BN columns, slot a part p at column
-// (a*NPART + p)*BN.  Partial accumulators come from MMA issuers that take
-// alternate K chunks of the unit; a unit of c chunks has min(c, NPART) of
-// them, and their sum is formed here in part order (0 + 1).
+// (a*NPART + p)*BN.  Partial accumulators come from MMA issuers that each
+// take kb_split of every kb_split*NPART consecutive K steps; part 1 exists
+// when the unit has more than kb_split K steps, and the parts are added
+// here in part order (0 + 1).
 template <int BN, int NACC = 2, int NPART = 1>
 __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, uint64_t *tfull, uint64_t *tempty,
-                                              volatile int *abort_flag, int warp, int lane, int kb_chunk = 1)
+                                              volatile int *abort_flag, int warp, int lane, int kb_split = 1)
 {
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -74,8 +75,7 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
         tc_fence_after();
         const int64_t n = static_cast<int64_t>(ui.tile / a.m_tiles) * kTileRows + row;
         const int64_t m0 = static_cast<int64_t>(ui.tile % a.m_tiles) * BN;
-        const int nchunks = (ui.kb1 - ui.kb0 + kb_chunk - 1) / kb_chunk;
-        const bool two = NPART == 2 && nchunks >= 2;
+        const bool two = NPART == 2 && ui.kb1 - ui.kb0 > kb_split;
         constexpr int kCols = BN < 32 ? BN : 32;   // columns per TMEM load
 #pragma unroll 1
         for (int c = 0; c < BN; c += kCols) {
