@@ -2,9 +2,11 @@
 """Prefill-GEMM benchmark of one Qwen2.5-7B-shaped layer on GB300.
 
 One step = the layer's seven prefill GEMMs Y = X . W^T at M = 2048 tokens
-through the library's public call mq_gemm_auto (the M gate sends M = 2048 to
-the cached path: tcgen05 GEMM on the f16 cache, split-K tail + fixed-order
-reduce where the tile grid underfills the GPU).  Weights q/k/v/o/gate/up are
+through the library's public calls: mq_gemm_grouped for the projections
+that share their input (q|k|v, gate|up: one launch each) and mq_gemm_auto
+for o and down (the M gate sends M = 2048 to the cached path).  All are the
+tcgen05 GEMM on the f16 cache, with a split-K tail + fixed-order reduce
+where a tile grid's last wave underfills the GPU.  Weights q/k/v/o/gate/up are
 Q4_K, down is Q6_K, all seeded synthetic bytes with the model's shapes; they
 are registered (decoded once into the f16 cache) before timing.
 
@@ -15,14 +17,18 @@ Printed: one JSON line (rank 0) with the contract keys plus
   cpu_baseline  the CPU oracle (f64) on a bounded sample of the same layer;
   e2e           the same metric with host buffers: pinned-host inputs copied
                 in and all outputs copied out inside the timed region;
-  decode        the one-time decoders (registration) against HBM bandwidth;
-  small_m       fused vs cached over the small-M sweep (crossover, HBM GB/s).
+  decode        the one-time decoders (registration, cold) against HBM bandwidth;
+  decode_steady the decoders back to back on the 7B gate/down shapes and a
+                Q8_0 weight of the gate's shape (HBM GB/s, fraction of peak);
+  small_m       fused vs cached over the small-M sweep, back to back over
+                rotating weight copies (crossover, HBM GB/s).
 
 --impl reference times the CPU oracle itself as the reference arm.
 """
 from __future__ import annotations
 
 import argparse
+import functools
 import hashlib
 import json
 import os
@@ -272,8 +278,7 @@ def main():
     mq.mq_reserve_workspace(64 << 20)
 
     def step(xmap):
-        for w, h, y in zip(weights, handles, ys):
-            mq.mq_gemm_auto(xmap[w.K], h, y, M_TOKENS, stream)
+        layer_step(mq, weights, handles, ys, xmap, M_TOKENS, stream)
 
     for _ in range(args.warmup):
         step(xdev)
@@ -311,14 +316,17 @@ def main():
     g_ms = sum(r["ms_main"] for r in gem)
     red_ms = sum(r["ms_aux"] for r in gem)
     per_gemm = []
-    for w in weights:
-        rs = [r for r in gem if r["N"] == w.N and r["K"] == w.K]
+    for grp in LAUNCH_GROUPS:
+        ws_ = [w for w in weights if w.name in grp]
+        n_tot, K_ = sum(w.N for w in ws_), ws_[0].K
+        rs = [r for r in gem if r["N"] == n_tot and r["K"] == K_]
         if rs:
             t_main = statistics.median(r["ms_main"] for r in rs)
             t_aux = statistics.median(r["ms_aux"] for r in rs)
-            per_gemm.append({"name": w.name, "N": w.N, "K": w.K, "type": synth.TYPE_NAME[w.qtype],
+            per_gemm.append({"name": "|".join(grp), "N": n_tot, "K": K_,
+                             "type": "/".join(sorted({synth.TYPE_NAME[w.qtype] for w in ws_})),
                              "gemm_us": t_main * 1e3, "reduce_us": t_aux * 1e3,
-                             "tflops": 2.0 * M_TOKENS * w.N * w.K / ((t_main + t_aux) * 1e-3) / 1e12})
+                             "tflops": 2.0 * M_TOKENS * n_tot * K_ / ((t_main + t_aux) * 1e-3) / 1e12})
     n_launch = max(1, len(gem))
     achieved = (g_flops / n_launch) / ((g_ms / n_launch) * 1e-3) / 1e12 if g_ms > 0 else None
     traffic = None
@@ -342,7 +350,8 @@ def main():
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M_TOKENS, "gemms": [w.name for w in weights],
                    "weights": "q/k/v/o/gate/up Q4_K, down Q6_K (seeded synthetic blocks, model shapes)",
-                   "gflop_per_step": flops_step / 1e9, "path": "mq_gemm_auto -> cached",
+                   "gflop_per_step": flops_step / 1e9,
+                   "path": "mq_gemm_grouped (q|k|v, gate|up) + mq_gemm_auto -> cached (o, down)",
                    "l2": "inputs larger than L2: 466 MB of f16 weight caches per step vs 126 MB L2",
                    "parallelism": f"replicas x{world} (independent token batches)"},
         "tok_per_s_per_layer": world * M_TOKENS / (ms * 1e-3),
@@ -361,6 +370,7 @@ def main():
     if not args.no_extras:
         out["e2e"] = e2e_run(mq, torch, weights, handles, xs, ys, stream, min(args.steps, 50), flops_step, dist)
         out["small_m"] = small_m_sweep(mq, torch, stream, P)
+        out["decode_steady"] = decode_steady(mq, torch, stream, P)
     if rank == 0 and world == 1 and not args.no_extras:
         tf, tokens, secs, dsec, threads = oracle_cpu_run(weights, xs, args.cpu_seconds)
         out["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -375,6 +385,23 @@ def main():
     return 0
 
 
+# The layer's GEMMs as launched: the projections that read the same
+# activations go out as one grouped launch (q|k|v on the attention input,
+# gate|up on the MLP input); o and down take the M gate (mq_gemm_auto).
+LAUNCH_GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
+
+
+def layer_step(mq, weights, handles, ys, xmap, M, stream):
+    by_name = {w.name: i for i, w in enumerate(weights)}
+    for grp in LAUNCH_GROUPS:
+        idx = [by_name[n] for n in grp]
+        x = xmap[weights[idx[0]].K]
+        if len(idx) == 1:
+            mq.mq_gemm_auto(x, handles[idx[0]], ys[idx[0]], M, stream)
+        else:
+            mq.mq_gemm_grouped(x, [handles[i] for i in idx], [ys[i] for i in idx], M, stream)
+
+
 def e2e_run(mq, torch, weights, handles, xs, ys, stream, steps, flops_step, dist):
     """Same step through the public API with host buffers: pinned host X
     copied in, all seven outputs copied back, inside the timed region."""
@@ -387,8 +414,7 @@ def e2e_run(mq, torch, weights, handles, xs, ys, stream, steps, flops_step, dist
     def step():
         for k in xh:
             xd[k].copy_(xh[k], non_blocking=True)
-        for w, h, y in zip(weights, handles, ys):
-            mq.mq_gemm_auto(xd[w.K], h, y, M_TOKENS, stream)
+        layer_step(mq, weights, handles, ys, xd, M_TOKENS, stream)
         for y, yhost in zip(ys, yh):
             yhost.copy_(y, non_blocking=True)
 
@@ -409,53 +435,86 @@ def e2e_run(mq, torch, weights, handles, xs, ys, stream, steps, flops_step, dist
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
 
+def _rotating_time_us(torch, fns, stream, reps=5):
+    """Median per-call device time of the calls in `fns`, issued back to back
+    on `stream` (CUDA events around the whole run of calls)."""
+    for fn in fns:
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for fn in fns:
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3 / len(fns))
+    return statistics.median(ts)
+
+
 def small_m_sweep(mq, torch, stream, P):
     """Fused vs cached on the 7B gate (Q4_K 18944x3584) and down (Q6_K
-    3584x18944) shapes, M in {1, 8, 32, 128, 512, 2048}: device time from
-    the library's trace events, cold L2 (a 256 MB buffer is written before
-    each timed call)."""
+    3584x18944) shapes over the M sweep.  Each point is the per-call time of
+    calls issued back to back over R registered copies of the weight, R chosen
+    so the weights touched (raw blocks for fused, f16 caches for cached) exceed
+    400 MB, three times the L2: every call streams its weight from HBM, as in
+    a layer stack, and the launch gap between calls is included."""
     weights, xs = synth.workload("small_m_sweep", seed=0)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     res = []
     for w in weights:
         if w.name == "up":
             continue
-        q = torch.from_numpy(w.data).cuda()
-        h = mq.mq_register_weight(w.qtype, q, w.N, w.K)
-        x_all = torch.from_numpy(xs[w.K]).cuda()
         raw_bytes = synth.nblocks(w.qtype, w.N, w.K) * synth.BLOCK[w.qtype][1]
+        R = max(3, -(-(400 << 20) // raw_bytes))
+        qs = [torch.from_numpy(w.data).cuda() for _ in range(R)]
+        hs = [mq.mq_register_weight(w.qtype, q, w.N, w.K) for q in qs]
+        x_all = torch.from_numpy(xs[w.K]).cuda()
         for M in synth.WORKLOADS["small_m_sweep"][1]:
             x = x_all[:M].contiguous()
             y = torch.empty((M, w.N), dtype=torch.float32, device="cuda")
-            row = {"name": w.name, "M": M}
-            for path, fn, kind in (("fused", mq.mq_gemm_fused, mq.MQ_TRACE_GEMM_FUSED),
-                                   ("cached", mq.mq_gemm, mq.MQ_TRACE_GEMM_CACHED)):
-                for _ in range(2):
-                    fn(x, h, y, M, stream)
-                ts = []
-                for _ in range(7):
-                    flush.zero_()
-                    mq.mq_trace_enable(True)
-                    fn(x, h, y, M, stream)
-                    torch.cuda.synchronize()
-                    r = mq.mq_trace_records()[-1]
-                    mq.mq_trace_enable(False)
-                    ts.append(r["ms_main"] + r["ms_aux"])
-                t = statistics.median(ts)
+            row = {"name": w.name, "M": M, "copies": R}
+            for path, fn in (("fused", mq.mq_gemm_fused), ("cached", mq.mq_gemm)):
+                calls = [functools.partial(fn, x, h, y, M, stream) for h in hs]
+                t_us = _rotating_time_us(torch, calls, stream)
                 wbytes = raw_bytes if path == "fused" else 2 * w.N * w.K
                 byts = wbytes + 2 * M * w.K + 4 * M * w.N
-                row[path + "_us"] = t * 1e3
-                row[path + "_tflops"] = 2.0 * M * w.N * w.K / (t * 1e-3) / 1e12
-                row[path + "_gbs"] = byts / (t * 1e-3) / 1e9
+                row[path + "_us"] = t_us
+                row[path + "_tflops"] = 2.0 * M * w.N * w.K / (t_us * 1e-6) / 1e12
+                row[path + "_gbs"] = byts / (t_us * 1e-6) / 1e9
                 row[path + "_frac_hbm"] = row[path + "_gbs"] / P["hbm_gbs"]
             res.append(row)
         mq.mq_stream_status()
-        h.release()
+        for h in hs:
+            h.release()
+        del qs
     cross = {}
     for name in ("gate", "down"):
         ms_ = [r["M"] for r in res if r["name"] == name and r["cached_us"] <= r["fused_us"]]
         cross[name] = min(ms_) if ms_ else None
-    return {"rows": res, "cached_wins_from_M": cross, "gate_in_use": mq.mq_get_m_gate()}
+    return {"rows": res, "cached_wins_from_M": cross, "gate_in_use": mq.mq_get_m_gate(),
+            "method": "back to back over rotating weight copies (> 3x L2), per-call average including launch gaps"}
+
+
+def decode_steady(mq, torch, stream, P):
+    """Standalone decoders (mq_dequantize) on the 7B gate (Q4_K), down (Q6_K)
+    and an 18944x3584 Q8_0 weight: per-call time of back-to-back calls over
+    three input copies into one f16 output (output 136 MB, larger than L2)."""
+    g = synth.rng(7)
+    out = {}
+    for qt, N, K in ((synth.Q4_K, 18944, 3584), (synth.Q6_K, 3584, 18944), (synth.Q8_0, 18944, 3584)):
+        data = synth.weight_bytes(g, qt, N, K)
+        qs = [torch.from_numpy(data).cuda() for _ in range(3)]
+        dst = torch.empty((N, K), dtype=torch.float16, device="cuda")
+        calls = [functools.partial(mq.mq_dequantize, qt, q, N, K, dst, None, stream) for q in qs] * 4
+        t_us = _rotating_time_us(torch, calls, stream)
+        byts = synth.nblocks(qt, N, K) * synth.BLOCK[qt][1] + 2 * N * K
+        out[synth.TYPE_NAME[qt]] = {"N": N, "K": K, "us": t_us, "bytes": byts,
+                                    "gbs": byts / (t_us * 1e-6) / 1e9,
+                                    "frac_hbm": byts / (t_us * 1e-6) / 1e9 / P["hbm_gbs"]}
+        del qs, dst
+    mq.mq_stream_status()
+    return out
 
 
 if __name__ == "__main__":

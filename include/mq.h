@@ -155,10 +155,37 @@ int mq_gemm(const void *x, mq_handle w, float *y, int64_t M, void *stream);
 int mq_gemm_fused(const void *x, mq_handle w, float *y, int64_t M, void *stream);
 
 /*
+ * mq_gemm_grouped -- the cached GEMM for `count` (1..4) weights that share K
+ * and the activations X, in one launch: y[g][M, N_g] = X . W_g^T for every
+ * member g.  ("Eager GPU Offload Without A Compute Graph", section "Storage
+ * and transfer reuse": a shared-input batch runs several weight matrices on
+ * the same activation rows without replicating them; here they also share
+ * one persistent tile schedule, so small members such as the k and v
+ * projections fill the GPU together with q instead of each needing split-K.)
+ *
+ * Arguments: x as for mq_gemm; w[0..count) handles registered with an f16
+ * cache, all with the same K and on the same device; y[0..count) caller-owned
+ * f32 outputs, y[g] of M x N_g, row-major, 16-byte aligned.  The members'
+ * outputs equal what mq_gemm computes for each, up to f32 summation order
+ * (a member may be split over K differently).  When every N_g is a multiple
+ * of 128 the call is one GEMM launch (plus one split-K reduction when the
+ * tile grid's last wave is split); otherwise the members run one after
+ * another with mq_gemm.
+ * Errors: MQ_ERR_INVALID (w or y NULL, count out of range, stale handle,
+ * members on different devices), MQ_ERR_NO_CACHE, MQ_ERR_SHAPE (K differs,
+ * bad M), MQ_ERR_ALIGN, and the errors of mq_gemm.  Nothing is launched when
+ * an argument check fails.
+ */
+int mq_gemm_grouped(const void *x, const mq_handle *w, int count, float *const *y, int64_t M, void *stream);
+
+/*
  * mq_gemm_auto -- M gate: fused when M < gate (and the handle allows it),
  * cached otherwise ("ggml-cuda: GEMM weight row padding ...", Summary: the
  * f16 path is a large-batch win; the threshold is a token count per call).
  * The gate is mq_get_m_gate(); environment variable MQ_M_GATE overrides it.
+ * Default 256: measured on GB300 with the 7B gate (Q4_K 18944x3584) and down
+ * (Q6_K 3584x18944) shapes, calls back to back over weights larger than L2,
+ * the fused path is faster up to M = 128 and the cached path from M = 256.
  */
 int mq_gemm_auto(const void *x, mq_handle w, float *y, int64_t M, void *stream);
 

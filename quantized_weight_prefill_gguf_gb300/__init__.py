@@ -25,7 +25,7 @@ STATUS = {0: "MQ_OK", -1: "MQ_ERR_INVALID", -2: "MQ_ERR_UNSUPPORTED_TYPE", -3: "
 EXPORTS = ("mq_register_weight", "mq_release_weight", "mq_weight_info", "mq_dequantize", "mq_gemm",
            "mq_gemm_fused", "mq_gemm_auto", "mq_get_m_gate", "mq_set_m_gate", "mq_reserve_workspace",
            "mq_stream_status", "mq_launch_count", "mq_error_string", "mq_last_error_detail", "mq_version",
-           "mq_trace_enable", "mq_trace_count", "mq_trace_read", "mq_gemm_noalloc")
+           "mq_trace_enable", "mq_trace_count", "mq_trace_read", "mq_gemm_noalloc", "mq_gemm_grouped")
 MQ_TRACE_GEMM_CACHED, MQ_TRACE_GEMM_FUSED, MQ_TRACE_DECODE = 1, 2, 3
 
 
@@ -52,6 +52,7 @@ def _load() -> ctypes.CDLL:
         "mq_gemm_fused": ([_P, _P, _P, _I64, _P], ctypes.c_int),
         "mq_gemm_auto": ([_P, _P, _P, _I64, _P], ctypes.c_int),
         "mq_gemm_noalloc": ([_P, _P, _P, _I64, _P], ctypes.c_int),
+        "mq_gemm_grouped": ([_P, ctypes.POINTER(_P), ctypes.c_int, ctypes.POINTER(_P), _I64, _P], ctypes.c_int),
         "mq_get_m_gate": ([], _I64),
         "mq_set_m_gate": ([_I64], ctypes.c_int),
         "mq_reserve_workspace": ([_I64], ctypes.c_int),
@@ -188,6 +189,17 @@ def mq_gemm_fused(x, w: Weight, y, M: int | None = None, stream=None) -> None:
 def mq_gemm_auto(x, w: Weight, y, M: int | None = None, stream=None) -> None:
     _check(_lib().mq_gemm_auto(_ptr(x), w.handle, _ptr(y), M if M is not None else x.shape[0], _stream(stream)),
            "mq_gemm_auto")
+
+
+def mq_gemm_grouped(x, ws, ys, M: int | None = None, stream=None) -> None:
+    """One cached GEMM launch for weights sharing K and X: ys[g] = x . ws[g]^T."""
+    if len(ws) != len(ys):
+        raise ValueError(f"{len(ws)} weights but {len(ys)} outputs")
+    n = len(ws)
+    harr = (_P * n)(*[w.handle for w in ws])
+    yarr = (_P * n)(*[_ptr(y) for y in ys])
+    _check(_lib().mq_gemm_grouped(_ptr(x), harr, n, yarr, M if M is not None else x.shape[0], _stream(stream)),
+           "mq_gemm_grouped")
 
 
 def mq_gemm_noalloc(x, w: Weight, y, M: int | None = None, stream=None) -> None:

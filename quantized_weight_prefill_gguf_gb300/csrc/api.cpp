@@ -219,25 +219,34 @@ int64_t env_int(const char *name, int64_t dflt)
     return (end && *end == '\0') ? x : dflt;
 }
 
-// Token count at and above which mq_gemm_auto takes the cached path.
+// Token count at and above which mq_gemm_auto takes the cached path: the
+// measured fused/cached crossover of the 7B gate and down shapes on GB300
+// (fused faster up to M = 128, cached from M = 256).
 int64_t current_gate()
 {
     int64_t g = g_gate.load();
     if (g > 0)
         return g;
-    return env_int("MQ_M_GATE", 64);
+    return env_int("MQ_M_GATE", 256);
 }
 
-// Plan, workspace and launch of one GEMM (cached or fused).
-int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bool fused)
+// Plan, workspace and launch of one GEMM: one weight (cached or fused), or a
+// group of weights that share K and X (cached; every member's N a multiple
+// of 128), run as one weight stacked along N.
+int run_gemm_group(const void *x, const mq_handle *ws, float *const *ys, int count, int64_t M, cudaStream_t s,
+                   bool fused)
 {
     DevState *d = nullptr;
     int rc = device_state(&d);
     if (rc)
         return rc;
+    const mq_handle w = ws[0];
+    int64_t n_total = 0;
+    for (int g = 0; g < count; ++g)
+        n_total += ws[g]->N;
 
     const bool splitk_on = env_int("MQ_SPLITK", 1) != 0;
-    const int64_t want = splitk_on ? mq::plan_ws_bytes_wanted(M, w->N, w->K, d->sms, fused) : 0;
+    const int64_t want = splitk_on ? mq::plan_ws_bytes_wanted(M, n_total, w->K, d->sms, fused) : 0;
     if (want > d->ws_bytes) {
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         cudaError_t e = cudaStreamIsCapturing(s, &cs);
@@ -250,7 +259,7 @@ int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bo
                 return rc;
         }
     }
-    const mq::GemmPlan plan = mq::plan_gemm(M, w->N, w->K, d->sms, fused, splitk_on ? d->ws_bytes : 0);
+    const mq::GemmPlan plan = mq::plan_gemm(M, n_total, w->K, d->sms, fused, splitk_on ? d->ws_bytes : 0);
 
     CUtensorMap tm_x;
     CUresult cr = mq::encode_f16_2d(&tm_x, x, M, w->K, w->K, 64, plan.bn);
@@ -259,28 +268,40 @@ int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bo
                     (long long)w->K, plan.bn, (int)cr);
 
     mq::GemmArgs a{};
-    a.y = y;
+    a.y = ys[0];
     a.ws = d->ws;
     a.status = d->status;
     a.wq = w->qdata;
     a.M = M;
-    a.N = w->N;
+    a.N = n_total;
     a.K = w->K;
     a.m_tiles = static_cast<int>((M + plan.bn - 1) / plan.bn);
-    a.n_tiles = static_cast<int>((w->N + 127) / 128);
     a.kblocks = static_cast<int>((w->K + 63) / 64);
     a.full_tiles = plan.full_tiles;
     a.split = plan.split;
     a.units = plan.units;
     a.kb_align = plan.kb_align;
     a.qtype = w->type;
+    a.groups = count;
+    mq::WMaps maps{};
+    int nt = 0;
+    for (int g = 0; g < count; ++g) {
+        a.g_tile0[g] = nt;
+        a.g_y[g] = ys[g];
+        a.g_N[g] = ws[g]->N;
+        nt += static_cast<int>((ws[g]->N + 127) / 128);
+        if (!fused)
+            maps.m[g] = ws[g]->tm_cache;
+    }
+    a.g_tile0[count] = nt;
+    a.n_tiles = nt;
 
     if (log_on())
-        fprintf(stderr, "[mq] %s M=%lld N=%lld K=%lld bn=%d tiles=%d split=%d full=%d units=%d grid=%d\n",
-                fused ? "fused" : "cached", (long long)M, (long long)w->N, (long long)w->K, plan.bn, plan.tiles,
-                plan.split, plan.full_tiles, plan.units, plan.grid);
+        fprintf(stderr, "[mq] %s M=%lld N=%lld K=%lld groups=%d bn=%d tiles=%d split=%d full=%d units=%d grid=%d\n",
+                fused ? "fused" : "cached", (long long)M, (long long)n_total, (long long)w->K, count, plan.bn,
+                plan.tiles, plan.split, plan.full_tiles, plan.units, plan.grid);
 
-    const int64_t tr = trace_begin(s, fused ? MQ_TRACE_GEMM_FUSED : MQ_TRACE_GEMM_CACHED, w->type, M, w->N, w->K);
+    const int64_t tr = trace_begin(s, fused ? MQ_TRACE_GEMM_FUSED : MQ_TRACE_GEMM_CACHED, w->type, M, n_total, w->K);
     a.raw_g = w->raw_g;
     a.raw_rb = w->K / w->qk * w->bb;
     // Failure injection for tests: the weight producer issues nothing, the
@@ -288,7 +309,7 @@ int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bo
     // mq_stream_status() reports MQ_ERR_DEVICE.
     a.stall_producer = env_int("MQ_INJECT_PRODUCER_STALL", 0) != 0 ? 1 : 0;
     cudaError_t e = fused ? mq::launch_gemm_fused(tm_x, w->raw_maps, a, plan, s)
-                          : mq::launch_gemm_cached(w->tm_cache, tm_x, a, plan, s);
+                          : mq::launch_gemm_cached(maps, tm_x, a, plan, s);
     if (e != cudaSuccess)
         return cuda_fail(e, fused ? "fused GEMM launch" : "cached GEMM launch");
     trace_mark(tr, 1, s);
@@ -297,6 +318,11 @@ int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bo
         return cuda_fail(e, "split-K reduce launch");
     trace_mark(tr, 2, s, plan.split > 1 && plan.tiles > plan.full_tiles);
     return MQ_OK;
+}
+
+int run_gemm(const void *x, mq_handle w, float *y, int64_t M, cudaStream_t s, bool fused)
+{
+    return run_gemm_group(x, &w, &y, 1, M, s, fused);
 }
 
 int check_gemm_args(const void *x, mq_handle w, float *y, int64_t M)
@@ -411,7 +437,14 @@ int gemm_cached_into_scratch(const void *x, mq_handle w, float *y, int64_t M, cu
     a.units = plan.units;
     a.kb_align = plan.kb_align;
     a.qtype = w->type;
-    e = launch_gemm_cached(w->tm_cache, tm_x, a, plan, s);
+    a.groups = 1;
+    a.g_tile0[0] = 0;
+    a.g_tile0[1] = a.n_tiles;
+    a.g_y[0] = y;
+    a.g_N[0] = w->N;
+    WMaps maps{};
+    maps.m[0] = w->tm_cache;
+    e = launch_gemm_cached(maps, tm_x, a, plan, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "cached GEMM launch");
     e = launch_splitk_reduce(a, plan, s);
@@ -616,6 +649,41 @@ int mq_gemm(const void *x, mq_handle w, float *y, int64_t M, void *stream)
     if (!w->cache)
         return fail(MQ_ERR_NO_CACHE, "weight was registered with MQ_REG_NO_CACHE; use mq_gemm_fused");
     return run_gemm(x, w, y, M, static_cast<cudaStream_t>(stream), false);
+}
+
+int mq_gemm_grouped(const void *x, const mq_handle *w, int count, float *const *y, int64_t M, void *stream)
+{
+    if (!w || !y)
+        return fail(MQ_ERR_INVALID, "%s is NULL", w ? "y" : "w");
+    if (count < 1 || count > mq::kMaxGroup)
+        return fail(MQ_ERR_INVALID, "count=%d: need 1 <= count <= %d", count, mq::kMaxGroup);
+    bool one_launch = true;
+    for (int g = 0; g < count; ++g) {
+        int rc = check_gemm_args(x, w[g], y[g], M);
+        if (rc)
+            return rc;
+        if (!w[g]->cache)
+            return fail(MQ_ERR_NO_CACHE, "member %d was registered with MQ_REG_NO_CACHE; grouped calls read the f16 cache", g);
+        if (w[g]->K != w[0]->K)
+            return fail(MQ_ERR_SHAPE, "member %d has K=%lld, member 0 has K=%lld: a group shares X", g,
+                        (long long)w[g]->K, (long long)w[0]->K);
+        if (w[g]->device != w[0]->device)
+            return fail(MQ_ERR_INVALID, "member %d is registered on device %d, member 0 on %d", g, w[g]->device,
+                        w[0]->device);
+        if (w[g]->N % 128 != 0)
+            one_launch = false;
+    }
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (one_launch || count == 1)
+        return run_gemm_group(x, w, y, count, M, s, false);
+    // A member whose N is not a multiple of the 128-row tile would share a
+    // tile with the next member: run the members one after another instead.
+    for (int g = 0; g < count; ++g) {
+        int rc = run_gemm(x, w[g], y[g], M, s, false);
+        if (rc)
+            return rc;
+    }
+    return MQ_OK;
 }
 
 int mq_gemm_fused(const void *x, mq_handle w, float *y, int64_t M, void *stream)

@@ -50,8 +50,7 @@ template <int BN> struct Cfg {
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_cached(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                  const GemmArgs a)
+    k_gemm_cached(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
 {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
@@ -86,7 +85,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&tm_w);
+        for (int g = 0; g < a.groups; ++g)
+            prefetch_tensormap(&tm_w.m[g]);
         prefetch_tensormap(&tm_x);
     }
     tc_fence_before();
@@ -103,7 +103,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = a.stall_producer == 0;
             for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
                 const UnitInfo ui = unit_info(a, u);
-                const int n0 = (ui.tile / a.m_tiles) * kTileRows;
+                const int nt = ui.tile / a.m_tiles;
+                const int g = group_of(a, nt);
+                const CUtensorMap *tmw = &tm_w.m[g];
+                const int n0 = (nt - a.g_tile0[g]) * kTileRows;   // row inside member g
                 const int m0 = (ui.tile % a.m_tiles) * BN;
                 for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
@@ -111,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full[stage], kABytes + C::kBBytes);
-                    tma_load_2d(sA + stage * kABytes, &tm_w, &full[stage], kb * kBK, n0);
+                    tma_load_2d(sA + stage * kABytes, tmw, &full[stage], kb * kBK, n0);
                     tma_load_2d(sB + stage * C::kBBytes, &tm_x, &full[stage], kb * kBK, m0);
                     issued |= 1u << stage;
                     issue_parity = (issue_parity & ~(1u << stage)) | (phase << stage);
@@ -205,9 +208,12 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(const GemmArgs a, int bn)
     if (e >= plane)
         return;
     const int col = e >> 7, row = e & 127;
+    const int nt = tile / a.m_tiles;
+    const int g = group_of(a, nt);
+    const int64_t Ng = a.g_N[g];
     const int64_t m = static_cast<int64_t>(tile % a.m_tiles) * bn + col;
-    const int64_t n = static_cast<int64_t>(tile / a.m_tiles) * kTileRows + row;
-    if (m >= a.M || n >= a.N)
+    const int64_t n = static_cast<int64_t>(nt - a.g_tile0[g]) * kTileRows + row;   // row inside member g
+    if (m >= a.M || n >= Ng)
         return;
     const float4 *base = reinterpret_cast<const float4 *>(a.ws + static_cast<int64_t>(slot) * a.split * plane + e);
     float4 v[kMaxSplit];
@@ -224,19 +230,18 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(const GemmArgs a, int bn)
             acc.z = __fadd_rn(acc.z, v[p].z);
             acc.w = __fadd_rn(acc.w, v[p].w);
         }
-    float *yp = a.y + m * a.N + n;
-    if ((a.N & 3) == 0 && n + 3 < a.N) {
+    float *yp = a.g_y[g] + m * Ng + n;
+    if ((Ng & 3) == 0 && n + 3 < Ng) {
         *reinterpret_cast<float4 *>(yp) = acc;
     } else {
         const float r[4] = {acc.x, acc.y, acc.z, acc.w};
-        for (int i = 0; i < 4 && n + i < a.N; ++i)
+        for (int i = 0; i < 4 && n + i < Ng; ++i)
             yp[i] = r[i];
     }
 }
 
 template <int BN>
-cudaError_t launch_bn(const CUtensorMap &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p,
-                      cudaStream_t s)
+cudaError_t launch_bn(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p, cudaStream_t s)
 {
     using C = Cfg<BN>;
     static bool attr_done[64] = {};   // the attribute is set once per device
@@ -305,7 +310,7 @@ int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fuse
     return plan_gemm(M, N, K, sms, fused, INT64_MAX).ws_bytes;
 }
 
-cudaError_t launch_gemm_cached(const CUtensorMap &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p,
+cudaError_t launch_gemm_cached(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p,
                                cudaStream_t s)
 {
     switch (p.bn) {
@@ -322,7 +327,7 @@ cudaError_t launch_splitk_reduce(const GemmArgs &a, const GemmPlan &p, cudaStrea
     const int slots = p.tiles - p.full_tiles;
     if (slots <= 0 || p.split <= 1)
         return cudaSuccess;
-    if (p.split > kMaxSplit)
+    if (p.split > kMaxSplit || a.groups < 1 || a.groups > kMaxGroup)
         return cudaErrorInvalidValue;
     k_splitk_reduce<<<dim3(p.bn / 8, slots), 256, 0, s>>>(a, p.bn);
     note_launch();

@@ -24,6 +24,13 @@ cudaError_t launch_dequant(int type, const void *q, int64_t nblocks, __half *out
 // all of K in one unit, the remaining tiles are split into `split` K-ranges
 // whose f32 partial planes go to the workspace and are summed in fixed
 // order p = 0..split-1 by the reduce kernel.
+// A grouped call runs several weights that share K and X in one launch, as
+// one weight stacked along N: member g owns n-tiles [g_tile0[g],
+// g_tile0[g+1]) (every member's N is a multiple of the 128-row tile, so a
+// tile never straddles two members), and its outputs go to g_y[g] [M, g_N[g]].
+// A single weight is the group of one (g_y[0] = y, g_N[0] = N).
+constexpr int kMaxGroup = 4;
+
 struct GemmArgs {
     float *y;            // [M, N] f32 output
     float *ws;           // split-K partial planes: [slot][part][BN][128]
@@ -45,6 +52,24 @@ struct GemmArgs {
     int64_t raw_rb;      // fused path: bytes per weight row (when rows start on block boundaries)
     int stall_producer;  // failure-injection hook: the weight producer issues nothing, so the
                          // consumers' bounded waits run out (tests of the timeout path)
+    int groups;                     // members of the group (1 for a single weight)
+    int g_tile0[kMaxGroup + 1];     // first n-tile of each member; g_tile0[groups] = n_tiles
+    float *g_y[kMaxGroup];          // member outputs
+    int64_t g_N[kMaxGroup];         // member row counts
+};
+
+// Member of the group that owns n-tile nt.
+__host__ __device__ inline int group_of(const GemmArgs &a, int nt)
+{
+    int g = 0;
+    while (g + 1 < a.groups && nt >= a.g_tile0[g + 1])
+        ++g;
+    return g;
+}
+
+// f16-cache tensor maps of the members of a group (one for a single weight).
+struct WMaps {
+    CUtensorMap m[kMaxGroup];
 };
 
 // Raw-weight tensor maps of a weight whose rows start on block boundaries
@@ -75,9 +100,9 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t
 // Workspace bytes the plan would use with an unlimited workspace.
 int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused);
 
-// Cached path: tm_w maps the f16 cache [N, ldk] (box 64 x 128), tm_x maps
-// X [M, K] (box 64 x bn).  Both 128-byte swizzled.
-cudaError_t launch_gemm_cached(const CUtensorMap &tm_w, const CUtensorMap &tm_x, const GemmArgs &a,
+// Cached path: tm_w.m[g] maps member g's f16 cache [N_g, ldk_g] (box 64 x
+// 128), tm_x maps X [M, K] (box 64 x bn).  All 128-byte swizzled.
+cudaError_t launch_gemm_cached(const WMaps &tm_w, const CUtensorMap &tm_x, const GemmArgs &a,
                                const GemmPlan &p, cudaStream_t s);
 
 // Fused path: tm_x as above; the weight is read from a.wq, through `maps`

@@ -73,7 +73,10 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
         if (!__all_sync(0xFFFFFFFFu, ok))
             break;
         tc_fence_after();
-        const int64_t n = static_cast<int64_t>(ui.tile / a.m_tiles) * kTileRows + row;
+        const int nt = ui.tile / a.m_tiles;
+        const int g = group_of(a, nt);
+        const int64_t Ng = a.g_N[g];
+        const int64_t n = static_cast<int64_t>(nt - a.g_tile0[g]) * kTileRows + row;   // row inside member g
         const int64_t m0 = static_cast<int64_t>(ui.tile % a.m_tiles) * BN;
         const bool two = NPART == 2 && ui.kb1 - ui.kb0 > kb_split;
         constexpr int kCols = BN < 32 ? BN : 32;   // columns per TMEM load
@@ -105,14 +108,14 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
             }
             tmem_ld_wait();
             if (ui.part < 0) {
-                if (n < a.N) {
-                    float *yp = a.y + (m0 + c) * a.N + n;
+                if (n < Ng) {
+                    float *yp = a.g_y[g] + (m0 + c) * Ng + n;
                     const int64_t rem = a.M - (m0 + c);
                     const int lim = rem < kCols ? static_cast<int>(rem) : kCols;
 #pragma unroll
                     for (int j = 0; j < kCols; ++j)
                         if (j < lim)
-                            yp[static_cast<int64_t>(j) * a.N] = __uint_as_float(r[j]);
+                            yp[static_cast<int64_t>(j) * Ng] = __uint_as_float(r[j]);
                 }
             } else {
                 float *wp = a.ws + ((static_cast<int64_t>(ui.slot) * a.split + ui.part) * BN + c) * kTileRows + row;
