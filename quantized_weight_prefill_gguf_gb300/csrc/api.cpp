@@ -246,7 +246,11 @@ int run_gemm_group(const void *x, const mq_handle *ws, float *const *ys, int cou
         n_total += ws[g]->N;
 
     const bool splitk_on = env_int("MQ_SPLITK", 1) != 0;
-    const int64_t want = splitk_on ? mq::plan_ws_bytes_wanted(M, n_total, w->K, d->sms, fused) : 0;
+    // Tuning override of the cached path's tile width (tokens per tile).
+    int bn_override = static_cast<int>(env_int("MQ_BN", 0));
+    if (bn_override != 32 && bn_override != 64 && bn_override != 128 && bn_override != 256)
+        bn_override = 0;
+    const int64_t want = splitk_on ? mq::plan_ws_bytes_wanted(M, n_total, w->K, d->sms, fused, bn_override) : 0;
     if (want > d->ws_bytes) {
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         cudaError_t e = cudaStreamIsCapturing(s, &cs);
@@ -259,7 +263,8 @@ int run_gemm_group(const void *x, const mq_handle *ws, float *const *ys, int cou
                 return rc;
         }
     }
-    const mq::GemmPlan plan = mq::plan_gemm(M, n_total, w->K, d->sms, fused, splitk_on ? d->ws_bytes : 0);
+    const mq::GemmPlan plan =
+        mq::plan_gemm(M, n_total, w->K, d->sms, fused, splitk_on ? d->ws_bytes : 0, bn_override);
 
     CUtensorMap tm_x;
     CUresult cr = mq::encode_f16_2d(&tm_x, x, M, w->K, w->K, 64, plan.bn);
@@ -350,6 +355,12 @@ int check_gemm_args(const void *x, mq_handle w, float *y, int64_t M)
 namespace mq {
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+bool pdl_enabled()
+{
+    static const bool on = env_int("MQ_PDL", 1) != 0;
+    return on;
+}
 
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,

@@ -34,6 +34,7 @@
 
 #include "mq_decode.cuh"
 #include "mq_internal.h"
+#include "mq_launch.cuh"
 #include "mq_ptx.cuh"
 
 namespace mq {
@@ -116,6 +117,8 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *__restrict_
         *reinterpret_cast<uint4 *>(sm + 16 * i) = ldg_nc_v4(src + 16 * i);
     for (int i = (n16 << 4) + threadIdx.x; i < bytes; i += kThreads)
         sm[i] = src[i];
+    grid_dep_launch();
+    grid_dep_wait();   // the output may be read by the previous kernel on the stream
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -224,10 +227,10 @@ cudaError_t launch_t(const void *q, int64_t nblocks, __half *out, int64_t K, int
         br.bpr = static_cast<uint32_t>(K / F::QK);
         br.m = 0xFFFFFFFFu / br.bpr;
     }
-    k_dequant<T><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(static_cast<const uint8_t *>(q), nblocks, out,
-                                                                  K, ldo, mode, br);
+    const cudaError_t e = launch_kernel(k_dequant<T>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
+                                        static_cast<const uint8_t *>(q), nblocks, out, K, ldo, mode, br);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace

@@ -56,6 +56,7 @@
 
 #include "mq_decode.cuh"
 #include "mq_internal.h"
+#include "mq_launch.cuh"
 #include "mq_ptx.cuh"
 #include "mq_smem.cuh"
 #include "mq_tile.cuh"
@@ -376,9 +377,11 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dep_launch();
 
     if (warp == 0) {
-        // ---------------- raw producer
+        // ---------------- raw producer (the raw blocks do not depend on the
+        // previous kernel on the stream: no grid_dep_wait here)
         int r = 0;
         uint32_t rphase = 0;
         uint32_t issued = 0, iparity = 0;
@@ -516,7 +519,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     } else if (warp == 2) {
         if (lane == 0) {
             // ---------------- activation-tile producer: chunk slot s is free
-            // again once the MMAs that read it are done.
+            // again once the MMAs that read it are done.  The activations may
+            // come from the previous kernel on the stream; Y is written only
+            // after MMAs that read them, so this wait also orders the stores.
+            grid_dep_wait();
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0, iparity = 0;
@@ -725,9 +731,9 @@ cudaError_t launch_f(const CUtensorMap &tx, const RawMaps &maps, const GemmArgs 
         if (dev >= 0 && dev < 64)
             attr_done[dev] = true;
     }
-    k_gemm_fused<BN, QT, TMA_RAW><<<p.grid, kThreadsF, L.smem, s>>>(tx, maps, a);
+    e = launch_kernel(k_gemm_fused<BN, QT, TMA_RAW>, dim3(p.grid), dim3(kThreadsF), L.smem, s, tx, maps, a);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 template <int QT, bool TMA_RAW>

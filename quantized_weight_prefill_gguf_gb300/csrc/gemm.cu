@@ -32,6 +32,7 @@
 #include <cuda_runtime.h>
 
 #include "mq_internal.h"
+#include "mq_launch.cuh"
 #include "mq_ptx.cuh"
 #include "mq_tile.cuh"
 
@@ -93,14 +94,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dep_launch();
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer
+            // ---------------- TMA producer.  The weight tiles of the first
+            // kStages K steps do not depend on the previous kernel on the
+            // stream, so they are requested before grid_dep_wait(); the
+            // activation tiles (and everything after) follow it.
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issue_parity = 0;   // per-stage: load in flight, its phase parity
             bool ok = a.stall_producer == 0;
+            int pre = 0;
+            for (int u = blockIdx.x; ok && pre < C::kStages && u < a.units; u += gridDim.x) {
+                const UnitInfo ui = unit_info(a, u);
+                const int nt = ui.tile / a.m_tiles;
+                const int g = group_of(a, nt);
+                const int n0 = (nt - a.g_tile0[g]) * kTileRows;
+                for (int kb = ui.kb0; kb < ui.kb1 && pre < C::kStages; ++kb, ++pre) {
+                    mbar_arrive_expect_tx(&full[pre], kABytes + C::kBBytes);
+                    tma_load_2d(sA + pre * kABytes, &tm_w.m[g], &full[pre], kb * kBK, n0);
+                    issued |= 1u << pre;
+                }
+            }
+            grid_dep_wait();
+            int step = 0;
             for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
                 const UnitInfo ui = unit_info(a, u);
                 const int nt = ui.tile / a.m_tiles;
@@ -108,7 +127,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const CUtensorMap *tmw = &tm_w.m[g];
                 const int n0 = (nt - a.g_tile0[g]) * kTileRows;   // row inside member g
                 const int m0 = (ui.tile % a.m_tiles) * BN;
-                for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
+                for (int kb = ui.kb0; kb < ui.kb1; ++kb, ++step) {
+                    if (step < pre) {
+                        // weight tile already requested (stage == step, phase 0)
+                        tma_load_2d(sB + stage * C::kBBytes, &tm_x, &full[stage], kb * kBK, m0);
+                        if (++stage == C::kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
                         ok = false;
                         break;
@@ -201,6 +229,8 @@ constexpr int kMaxSplit = 8;
 
 __global__ void __launch_bounds__(256) k_splitk_reduce(const GemmArgs a, int bn)
 {
+    grid_dep_launch();
+    grid_dep_wait();   // the partial planes come from the GEMM kernel just before
     const int slot = blockIdx.y;
     const int tile = a.full_tiles + slot;
     const int64_t plane = static_cast<int64_t>(bn) * kTileRows;
@@ -256,14 +286,14 @@ cudaError_t launch_bn(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a,
         if (dev >= 0 && dev < 64)
             attr_done[dev] = true;
     }
-    k_gemm_cached<BN><<<p.grid, kThreads, C::kSmem, s>>>(tw, tx, a);
+    e = launch_kernel(k_gemm_cached<BN>, dim3(p.grid), dim3(kThreads), C::kSmem, s, tw, tx, a);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace
 
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available)
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available, int bn_override)
 {
     GemmPlan p{};
     // The fused path keeps a whole 256-element K chunk of activations per
@@ -273,6 +303,8 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t
         p.bn = M > 64 ? 128 : (M > 32 ? 64 : (M > 16 ? 32 : 16));
     else
         p.bn = M > 128 ? 256 : (M > 64 ? 128 : (M > 32 ? 64 : 32));
+    if (!fused && bn_override > 0)
+        p.bn = bn_override;
     // The fused path stages raw weight bytes 256 K-elements (4 K steps) at a
     // time, so its split boundaries fall on multiples of 4 K steps.
     p.kb_align = fused ? 4 : 1;
@@ -305,9 +337,9 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t
     return p;
 }
 
-int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused)
+int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused, int bn_override)
 {
-    return plan_gemm(M, N, K, sms, fused, INT64_MAX).ws_bytes;
+    return plan_gemm(M, N, K, sms, fused, INT64_MAX, bn_override).ws_bytes;
 }
 
 cudaError_t launch_gemm_cached(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p,
@@ -329,9 +361,9 @@ cudaError_t launch_splitk_reduce(const GemmArgs &a, const GemmPlan &p, cudaStrea
         return cudaSuccess;
     if (p.split > kMaxSplit || a.groups < 1 || a.groups > kMaxGroup)
         return cudaErrorInvalidValue;
-    k_splitk_reduce<<<dim3(p.bn / 8, slots), 256, 0, s>>>(a, p.bn);
+    const cudaError_t e = launch_kernel(k_splitk_reduce, dim3(p.bn / 8, slots), dim3(256), 0, s, a, p.bn);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace mq

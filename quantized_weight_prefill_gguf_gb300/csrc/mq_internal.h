@@ -95,10 +95,12 @@ struct GemmPlan {
 };
 
 // Choose tile width, split-K and grid for an M x N x K problem on `sms` SMs.
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available);
+// bn_override > 0 forces the cached path's tile width (32, 64, 128 or 256).
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available,
+                   int bn_override = 0);
 
 // Workspace bytes the plan would use with an unlimited workspace.
-int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused);
+int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused, int bn_override = 0);
 
 // Cached path: tm_w.m[g] maps member g's f16 cache [N_g, ldk_g] (box 64 x
 // 128), tm_x maps X [M, K] (box 64 x bn).  All 128-byte swizzled.

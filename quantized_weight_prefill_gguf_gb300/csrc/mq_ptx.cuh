@@ -45,6 +45,24 @@ __device__ __forceinline__ void fence_barrier_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- launch order
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream is still
+// running.  grid_dep_wait() blocks until that kernel has completed and its
+// memory is visible (it returns at once when there is none); everything that
+// reads data the previous kernel may produce, or writes memory it may read,
+// comes after it.  grid_dep_launch() lets the next kernel on the stream start
+// (its blocks begin as this kernel's blocks leave the SMs).
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
