@@ -67,7 +67,7 @@ def peaks():
 def cached_kernel_source_hash() -> str:
     """sha256 over the sources that make up the cached GEMM kernel."""
     h = hashlib.sha256()
-    for f in ("gemm.cu", "mq_tile.cuh", "mq_ptx.cuh"):
+    for f in ("gemm.cu", "mq_tile.cuh", "mq_ptx.cuh", "mq_internal.h", "mq_launch.cuh"):
         with open(os.path.join(ROOT, "quantized_weight_prefill_gguf_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
