@@ -38,8 +38,9 @@
 //               an MMA is a short chain of dependent instructions competing
 //               with the decode warps for issue slots, and one thread alone
 //               leaves the tensor pipe idle between MMAs.
-//   warp 2      activation producer (TMA): the BN x 256 activations of a
-//               chunk (four 64-wide boxes) into the chunk slot's X stage.
+//   warp 2      activation producer (TMA, lane 0): the BN x 256 activations
+//               of a chunk (four 64-wide boxes) into the chunk slot's X
+//               stage; lane 1 announces each slot's landed activations.
 //   warps 4-7   epilogue (TMEM -> Y / split-K workspace; sums the partial
 //               accumulators in a fixed order).
 //   warps 8-15  decoders: thread (row, pair of K steps) turns 128 raw
@@ -49,8 +50,9 @@
 //               the MMA issuers (measured: ~86 cycles per MMA next to 8 busy
 //               warps, ~220 next to 30).
 // Chunk slots: A stage s (TMEM) and X stage s (shared memory) form one slot;
-// `ready[s]` completes when the decoders have written A and the activations
-// have landed, `done[s]` (an MMA commit) frees both.
+// `ready[s]` completes when the decoder warps have written A and a second
+// thread of warp 2 has seen the slot's activations land; `done[s]` (an MMA
+// commit) frees both.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -351,7 +353,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         }
         for (int s = 0; s < S; ++s) {
             mbar_init(&x_full[s], 1);
-            mbar_init(&ready[s], kDecodeWarps);
+            mbar_init(&ready[s], kDecodeWarps + 1);
             mbar_init(&done[s], kIssuers);
         }
         for (int i = 0; i < kNAcc; ++i) {
@@ -553,6 +555,27 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                     if (issued & (1u << i))
                         mbar_wait_bounded(&x_full[i], (iparity >> i) & 1u, &no_abort, a.status);
             }
+        } else if (lane == 1) {
+            // ---------------- announcer: in chunk order, once a slot's
+            // activations have landed, the one extra arrival `ready` waits
+            // for (the decoders never wait for X themselves).
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
+                const UnitInfo ui = unit_info(a, u);
+                for (int kb = ui.kb0; kb < ui.kb1; kb += kChunkSteps) {
+                    if (!mbar_wait_bounded(&x_full[s], ph, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive(&ready[s]);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
         }
     } else if (warp >= 4 && warp < 8) {
         // ---------------- epilogue: warps 4..7 own TMEM lane quarters 0..3
@@ -562,9 +585,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         // (the TMEM lanes it may access) and kStepsPerThread K steps from
         // j0 = kStepsPerThread*((w-8)/4) of every chunk: thread (row, j0)
         // writes the f16 of its row for those steps into TMEM lane `row`,
-        // columns 32*j0 .. of the chunk's A stage.  The first decoder warp also waits for the
-        // chunk's activations before it arrives, so `ready` means "A decoded
-        // and X landed".
+        // columns 32*j0 .. of the chunk's A stage.
         const int dw = warp - kDecodeWarp0;
         const int row = (warp & 3) * 32 + lane;
         const int j0 = kStepsPerThread * (dw >> 2);
@@ -634,18 +655,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                bool xok = true;
-                if (dw == 0 && lane == 0)
-                    xok = mbar_wait_bounded(&x_full[s], ph, abort_flag, a.status);
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&raw_empty[r]);
-                    if (xok)
-                        mbar_arrive(&ready[s]);
-                }
-                if (!__shfl_sync(0xFFFFFFFFu, xok, 0)) {
-                    ok = false;
-                    break;
+                    mbar_arrive(&ready[s]);
                 }
                 if (++s == S) {
                     s = 0;

@@ -163,8 +163,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---------------- MMA issuer
+            // ---------------- MMA issuer.  Descriptors are precomputed, so
+            // only adds sit between consecutive MMAs of a stage.  (Waiting
+            // for the next stage before the current stage's last MMA was
+            // measured slower: it delays the commit that frees the stage.)
             constexpr uint32_t idesc = idesc_f16_f32(kTileRows, BN);
+            const uint64_t a_desc0 = sdesc_k_sw128(smem_u32(sA));
+            const uint64_t b_desc0 = sdesc_k_sw128(smem_u32(sB));
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -182,12 +187,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sA + stage * kABytes);
-                    const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
+                    // descriptor start fields are 16-byte units (14 bits): shared
+                    // addresses stay below 256 KB, so adding the stage offset
+                    // never carries out of the field
+                    const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * kABytes) >> 4);
+                    const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * C::kBBytes) >> 4);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)
-                        umma_f16(d_tmem, sdesc_k_sw128(a_addr + 32 * k), sdesc_k_sw128(b_addr + 32 * k), idesc,
-                                 (kb > ui.kb0 || k > 0) ? 1u : 0u);
+                        umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > ui.kb0 || k > 0) ? 1u : 0u);
                     umma_commit(&empty[stage]);
                     if (++stage == C::kStages) {
                         stage = 0;
