@@ -108,14 +108,6 @@ template <> struct QF<8> { static constexpr int QK = 32, BB = 34; };
 template <> struct QF<12> { static constexpr int QK = 256, BB = 144; };
 template <> struct QF<14> { static constexpr int QK = 256, BB = 210; };
 
-// Shared-memory bytes per row of a raw stage on the tensor-map path: one
-// 256-element chunk plus up to 14 bytes of leading misalignment, rounded to
-// 16 (Q4_K chunks are always aligned).
-template <int QT> constexpr int tma_row_bytes()
-{
-    return QT == 12 ? 144 : (QT == 14 ? 224 : 272);
-}
-
 struct RowSpan {
     int64_t s0;       // 16-byte-aligned start of the copied range in the stream
     uint32_t bytes;   // multiple of 16

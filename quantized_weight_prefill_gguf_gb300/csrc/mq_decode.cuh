@@ -29,12 +29,6 @@ __device__ __forceinline__ float small_uint_to_f32(uint32_t v)
     return __int_as_float(0x4B000000u | v) - 8388608.0f;
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
-{
-    __half2 h = __floats2half2_rn(lo, hi);   // .x (low 16 bits) = lo
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
 __device__ __forceinline__ float f16_bits_to_f32(uint32_t bits16)
 {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
