@@ -44,11 +44,21 @@
 extern "C" {
 #endif
 
-/* GGUF type ids of the supported block formats. */
+/* GGUF type ids of the supported block formats.  The pages name the types;
+ * field layouts are the GGUF convention ("05 · 8p — Persistent f16 weight
+ * cache + fused dequant-in-GEMM", sections 1-2 give Q5_0's fields and the
+ * block sizes). */
 typedef enum {
+    MQ_TYPE_Q4_0 = 2,   /* 32 elements in 18 bytes: f16 d, 16 B of 4-bit quants (q - 8) */
+    MQ_TYPE_Q5_0 = 6,   /* 32 elements in 22 bytes: f16 d, 4 B fifth-bit plane, 16 B of
+                           low 4 bits (q - 16); 2-byte aligned blocks                   */
+    MQ_TYPE_Q5_1 = 7,   /* 32 elements in 24 bytes: f16 d, f16 m, 4 B fifth-bit plane,
+                           16 B of low 4 bits (d*q + m)                                */
     MQ_TYPE_Q8_0 = 8,   /* 32 elements in 34 bytes: f16 d, int8 q[32]                 */
     MQ_TYPE_Q4_K = 12,  /* 256 elements in 144 bytes: f16 d, f16 dmin, 12 B of 6-bit
                            scales/mins, 128 B of 4-bit quants                          */
+    MQ_TYPE_Q5_K = 13,  /* 256 elements in 176 bytes: as Q4_K plus 32 B of fifth bits
+                           (bit s of byte i belongs to sub-block s, position i)        */
     MQ_TYPE_Q6_K = 14   /* 256 elements in 210 bytes: 128 B low nibbles, 64 B high
                            2-bit fields, 16 int8 scales, f16 d                          */
 } mq_type;
@@ -56,7 +66,7 @@ typedef enum {
 /* Status codes. */
 #define MQ_OK                    0
 #define MQ_ERR_INVALID          -1  /* null pointer, unknown or released handle, bad flag  */
-#define MQ_ERR_UNSUPPORTED_TYPE -2  /* type id is not Q8_0 / Q4_K / Q6_K                  */
+#define MQ_ERR_UNSUPPORTED_TYPE -2  /* type id is not one of the mq_type block formats      */
 #define MQ_ERR_SHAPE            -3  /* a size precondition does not hold                   */
 #define MQ_ERR_ALIGN            -4  /* a pointer is not 16-byte aligned                    */
 #define MQ_ERR_NO_CACHE         -5  /* mq_gemm on a handle registered with MQ_REG_NO_CACHE */

@@ -18,6 +18,11 @@
  *      types and their bytes per weight only ("05 · 8p", section 1); the
  *      block sizes 34 / 144 / 210 bytes and the field layout follow the
  *      GGUF format convention (a reading: no page prints the layout).
+ *      Also Q4_0 / Q5_0 / Q5_1 / Q5_K (18 / 22 / 24 / 176 bytes): the pages
+ *      give Q5_0's fields (f16 d, 4-byte qh bit plane, 16 nibble bytes;
+ *      "05 · 8p", section 2) and Q5_1's size, and name Q4_0 and Q5_K's
+ *      bit-transposed qh ("79 · Phase-8 coverage & first-measurement
+ *      batch", section 3.4); the rest of each layout is the GGUF convention.
  *      Arithmetic is binary32 in the fixed order d*sc*q - dmin*m, then one
  *      round-to-nearest to binary16, as the dequant kernel shown in
  *      "05 · 8p", section 3.2 does (f32 product, then __float2half).
@@ -112,7 +117,7 @@ uint16_t oracle_f32_to_f16(float f)
 /* O2: block decoders                                                 */
 /* ------------------------------------------------------------------ */
 
-enum { T_Q8_0 = 8, T_Q4_K = 12, T_Q6_K = 14 };
+enum { T_Q4_0 = 2, T_Q5_0 = 6, T_Q5_1 = 7, T_Q8_0 = 8, T_Q4_K = 12, T_Q5_K = 13, T_Q6_K = 14 };
 
 static uint16_t rd_u16le(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
 
@@ -201,12 +206,90 @@ static void decode_q6_K_block(const uint8_t *b, uint16_t *y)
     }
 }
 
+/* Q4_0, 18 bytes: d (f16) at 0, qs[16] at 2.  Element j (0..15) is the low
+ * nibble of qs[j], element j+16 the high nibble; both offset by -8.
+ *   y = RN16(d * (nibble - 8)) */
+static void decode_q4_0_block(const uint8_t *b, uint16_t *y)
+{
+    float d = oracle_f16_to_f32(rd_u16le(b));
+    const uint8_t *qs = b + 2;
+    for (int e = 0; e < 32; e++) {
+        int nib = e < 16 ? (qs[e] & 15) : (qs[e - 16] >> 4);
+        y[e] = oracle_f32_to_f16(d * (float)(nib - 8));
+    }
+}
+
+/* The 5-bit value of element e (0..31) of a Q5_0 / Q5_1 block: nibble as
+ * in Q4_0 (qs[e] low, qs[e-16] high), fifth bit = bit e of the 32-bit
+ * little-endian bit plane qh ("05 · 8p", section 2: a 4-byte qh bit plane
+ * after the f16 d, then 16 nibble bytes). */
+static int q5_value(const uint8_t *qh, const uint8_t *qs, int e)
+{
+    uint32_t h = (uint32_t)qh[0] | ((uint32_t)qh[1] << 8) | ((uint32_t)qh[2] << 16) | ((uint32_t)qh[3] << 24);
+    int nib = e < 16 ? (qs[e] & 15) : (qs[e - 16] >> 4);
+    return nib | (int)(((h >> e) & 1u) << 4);
+}
+
+/* Q5_0, 22 bytes: d (f16) at 0, qh[4] at 2, qs[16] at 6.
+ *   y = RN16(d * (q5 - 16)) */
+static void decode_q5_0_block(const uint8_t *b, uint16_t *y)
+{
+    float d = oracle_f16_to_f32(rd_u16le(b));
+    for (int e = 0; e < 32; e++)
+        y[e] = oracle_f32_to_f16(d * (float)(q5_value(b + 2, b + 6, e) - 16));
+}
+
+/* Q5_1, 24 bytes: d (f16) at 0, m (f16) at 2, qh[4] at 4, qs[16] at 8.
+ *   y = RN16( RN32(RN32(d * q5) + m) ) */
+static void decode_q5_1_block(const uint8_t *b, uint16_t *y)
+{
+    float d = oracle_f16_to_f32(rd_u16le(b));
+    float m = oracle_f16_to_f32(rd_u16le(b + 2));
+    for (int e = 0; e < 32; e++) {
+        float dq = d * (float)q5_value(b + 4, b + 8, e);
+        y[e] = oracle_f32_to_f16(dq + m);
+    }
+}
+
+/* Q5_K, 176 bytes: d (f16) at 0, dmin (f16) at 2, S[12] at 4 (packed as in
+ * Q4_K), qh[32] at 16, qs[128] at 48.  Group p = 0..3 covers elements
+ * 64p .. 64p+63: element 64p+i (i < 32) is the low nibble of qs[32p+i]
+ * with fifth bit = bit 2p of qh[i], sub-block 2p; element 64p+32+i is the
+ * high nibble of the same byte with fifth bit = bit 2p+1 of qh[i], sub-block
+ * 2p+1 (qh is bit-transposed: bit s of byte i belongs to sub-block s).
+ *   y = RN16( RN32( RN32(RN32(d*sc)*q) - RN32(dmin*m) ) ) */
+static void decode_q5_K_block(const uint8_t *b, uint16_t *y)
+{
+    float d = oracle_f16_to_f32(rd_u16le(b));
+    float dmin = oracle_f16_to_f32(rd_u16le(b + 2));
+    const uint8_t *S = b + 4;
+    const uint8_t *qh = b + 16;
+    const uint8_t *qs = b + 48;
+    for (int e = 0; e < 256; e++) {
+        int grp = e / 64;            /* group p */
+        int upper = (e % 64) >= 32;  /* high nibbles */
+        int pos = e % 32;
+        int sub = 2 * grp + upper;
+        int nib = upper ? (qs[32 * grp + pos] >> 4) : (qs[32 * grp + pos] & 15);
+        int q5 = nib | (((qh[pos] >> sub) & 1) << 4);
+        int scale, mn;
+        q4k_scale_min(S, sub, &scale, &mn);
+        float prod = (d * (float)scale) * (float)q5;
+        float off = dmin * (float)mn;
+        y[e] = oracle_f32_to_f16(prod - off);
+    }
+}
+
 /* Elements per block (QK) and bytes per block for a GGUF type id. */
 int oracle_block_size(int type, int *qk, int *bytes)
 {
     switch (type) {
+    case T_Q4_0: *qk = 32;  *bytes = 18;  return 0;
+    case T_Q5_0: *qk = 32;  *bytes = 22;  return 0;
+    case T_Q5_1: *qk = 32;  *bytes = 24;  return 0;
     case T_Q8_0: *qk = 32;  *bytes = 34;  return 0;
     case T_Q4_K: *qk = 256; *bytes = 144; return 0;
+    case T_Q5_K: *qk = 256; *bytes = 176; return 0;
     case T_Q6_K: *qk = 256; *bytes = 210; return 0;
     default: return -1;
     }
@@ -224,12 +307,15 @@ int oracle_decode(int type, const uint8_t *q, int64_t nblocks, uint16_t *out)
     for (int64_t i = 0; i < nblocks; i++) {
         const uint8_t *b = q + i * bb;
         uint16_t *y = out + i * qk;
-        if (type == T_Q8_0)
-            decode_q8_0_block(b, y);
-        else if (type == T_Q4_K)
-            decode_q4_K_block(b, y);
-        else
-            decode_q6_K_block(b, y);
+        switch (type) {
+        case T_Q4_0: decode_q4_0_block(b, y); break;
+        case T_Q5_0: decode_q5_0_block(b, y); break;
+        case T_Q5_1: decode_q5_1_block(b, y); break;
+        case T_Q8_0: decode_q8_0_block(b, y); break;
+        case T_Q4_K: decode_q4_K_block(b, y); break;
+        case T_Q5_K: decode_q5_K_block(b, y); break;
+        default:     decode_q6_K_block(b, y); break;
+        }
     }
     return 0;
 }

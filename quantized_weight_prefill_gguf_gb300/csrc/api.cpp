@@ -132,8 +132,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool block_format(int type, int &qk, int &bb)
 {
     switch (type) {
+    case MQ_TYPE_Q4_0: qk = 32; bb = 18; return true;
+    case MQ_TYPE_Q5_0: qk = 32; bb = 22; return true;
+    case MQ_TYPE_Q5_1: qk = 32; bb = 24; return true;
     case MQ_TYPE_Q8_0: qk = 32; bb = 34; return true;
     case MQ_TYPE_Q4_K: qk = 256; bb = 144; return true;
+    case MQ_TYPE_Q5_K: qk = 256; bb = 176; return true;
     case MQ_TYPE_Q6_K: qk = 256; bb = 210; return true;
     default: return false;
     }
@@ -500,7 +504,8 @@ int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, ui
     int qk = 0, bb = 0;
     if (!block_format(type, qk, bb))
         return fail(MQ_ERR_UNSUPPORTED_TYPE,
-                    "type id %d is not supported (supported: Q8_0=8, Q4_K=12, Q6_K=14); the weight has no kernel",
+                    "type id %d is not supported (supported: Q4_0=2, Q5_0=6, Q5_1=7, Q8_0=8, Q4_K=12, Q5_K=13, "
+                    "Q6_K=14); the weight has no kernel",
                     (int)type);
     if (flags & ~(MQ_REG_NO_CACHE | MQ_REG_NO_KPAD | MQ_REG_KPAD))
         return fail(MQ_ERR_INVALID, "unknown flag bits 0x%x", flags);
@@ -628,7 +633,9 @@ int mq_dequantize(mq_type type, const void *qdata, int64_t N, int64_t K, void *o
 {
     int qk = 0, bb = 0;
     if (!block_format(type, qk, bb))
-        return fail(MQ_ERR_UNSUPPORTED_TYPE, "type id %d is not supported (Q8_0=8, Q4_K=12, Q6_K=14)", (int)type);
+        return fail(MQ_ERR_UNSUPPORTED_TYPE,
+                    "type id %d is not supported (Q4_0=2, Q5_0=6, Q5_1=7, Q8_0=8, Q4_K=12, Q5_K=13, Q6_K=14)",
+                    (int)type);
     if (!qdata || !out_f16)
         return fail(MQ_ERR_INVALID, "%s is NULL", qdata ? "out_f16" : "qdata");
     if (N < 1 || K < 8 || (K % 8) != 0 || ldo < K || (ldo % 8) != 0)

@@ -43,9 +43,13 @@ namespace {
 template <int T> struct Fmt;
 // QK elements per block, BB bytes per block, BPG blocks per lane group, G
 // blocks per CTA span (G * BB is a multiple of 16).
-template <> struct Fmt<8> { static constexpr int QK = 32, BB = 34, BPG = 16, G = 256; };    // span 8704 B
-template <> struct Fmt<12> { static constexpr int QK = 256, BB = 144, BPG = 2, G = 32; };   // span 4608 B
-template <> struct Fmt<14> { static constexpr int QK = 256, BB = 210, BPG = 2, G = 32; };   // span 6720 B
+template <> struct Fmt<2> { static constexpr int QK = 32, BB = 18, BPG = 16, G = 256; };    // Q4_0, span 4608 B
+template <> struct Fmt<6> { static constexpr int QK = 32, BB = 22, BPG = 16, G = 256; };    // Q5_0, span 5632 B
+template <> struct Fmt<7> { static constexpr int QK = 32, BB = 24, BPG = 16, G = 256; };    // Q5_1, span 6144 B
+template <> struct Fmt<8> { static constexpr int QK = 32, BB = 34, BPG = 16, G = 256; };    // Q8_0, span 8704 B
+template <> struct Fmt<12> { static constexpr int QK = 256, BB = 144, BPG = 2, G = 32; };   // Q4_K, span 4608 B
+template <> struct Fmt<13> { static constexpr int QK = 256, BB = 176, BPG = 2, G = 32; };   // Q5_K, span 5632 B
+template <> struct Fmt<14> { static constexpr int QK = 256, BB = 210, BPG = 2, G = 32; };   // Q6_K, span 6720 B
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *__restrict_
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if constexpr (T == 12) {
+    if constexpr (T == 12 || T == 13) {
         // Lane pair (2j, 2j+1) of a 16-lane half owns sub-block s = j of one
         // block: 32 elements with one (scale, min); lane h = 0/1 of the pair
         // takes elements 32s + 8h + {0..7} and 32s + 16 + 8h + {0..7}, whose
@@ -132,7 +136,11 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *__restrict_
         const int nsh = (sub & 1) * 4;
         const int bsel = (sub & 3) * 8;                 // byte j = s mod 4 of the scale words
         const bool upper = sub >= 4;
-        const int qoff = 16 + 32 * (sub >> 1) + 8 * h;
+        // Q5_K: qs starts at byte 48 and the fifth bit of position i of
+        // sub-block s is bit s of qh[i] (qh at byte 16), rotated onto bit 4.
+        const int qoff = (T == 12 ? 16 : 48) + 32 * (sub >> 1) + 8 * h;
+        const int qhoff = 16 + 8 * h;
+        const int hrot = (sub + 28) & 31;
         const int eoff = 32 * sub + 8 * h;
 #pragma unroll
         for (int ps = 0; ps < kPasses; ++ps) {
@@ -151,8 +159,21 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *__restrict_
                 const uint32_t mn = upper ? ((c >> 4) | ((bm >> 2) & 0x30u)) : (bm & 63u);
                 const float A = __fmul_rn(f16_bits_to_f32(hd.x), small_uint_to_f32(sc));
                 const float B = __fmul_rn(f16_bits_to_f32(hd.x >> 16), small_uint_to_f32(mn));
-                const uint4 y0 = q4k_eight(A, B, w0.x, w0.y, nsh);
-                const uint4 y1 = q4k_eight(A, B, w1.x, w1.y, nsh);
+                uint4 y0, y1;
+                if constexpr (T == 12) {
+                    y0 = q4k_eight(A, B, w0.x, w0.y, nsh);
+                    y1 = q4k_eight(A, B, w1.x, w1.y, nsh);
+                } else {
+                    const uint2 h0 = *reinterpret_cast<const uint2 *>(b + qhoff);
+                    const uint2 h1 = *reinterpret_cast<const uint2 *>(b + qhoff + 16);
+                    const uint64_t a2 = f32x2(A, A), nb2 = f32x2(-B, -B);
+                    y0 = fma_bytes_eight(a2, nb2,
+                                         ((w0.x >> nsh) & 0x0F0F0F0Fu) | (__funnelshift_r(h0.x, h0.x, hrot) & 0x10101010u),
+                                         ((w0.y >> nsh) & 0x0F0F0F0Fu) | (__funnelshift_r(h0.y, h0.y, hrot) & 0x10101010u));
+                    y1 = fma_bytes_eight(a2, nb2,
+                                         ((w1.x >> nsh) & 0x0F0F0F0Fu) | (__funnelshift_r(h1.x, h1.x, hrot) & 0x10101010u),
+                                         ((w1.y >> nsh) & 0x0F0F0F0Fu) | (__funnelshift_r(h1.y, h1.y, hrot) & 0x10101010u));
+                }
                 const uint32_t bi = static_cast<uint32_t>(b0 + blk);
                 stg_v4(dest<F::QK>(out, bi, eoff, mode, K, ldo, br), y0);
                 stg_v4(dest<F::QK>(out, bi, eoff + 16, mode, K, ldo, br), y1);
@@ -190,6 +211,49 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *__restrict_
                 const uint32_t bi = static_cast<uint32_t>(b0 + blk);
                 stg_v4(dest<F::QK>(out, bi, eoff, mode, K, ldo, br), y0);
                 stg_v4(dest<F::QK>(out, bi, eoff + 16, mode, K, ldo, br), y1);
+            }
+        }
+    } else if constexpr (T == 2 || T == 6 || T == 7) {
+        // Q4_0 / Q5_0 / Q5_1.  Lane pair j owns block j of the group; lane h
+        // takes elements 8h + {0..7} (low nibbles of qs[8h..8h+7]) and
+        // 16 + 8h + {0..7} (high nibbles of the same bytes).  Q5_0 / Q5_1 add
+        // bit e of the 32-bit qh plane as the fifth bit of element e.
+        constexpr int kQh = T == 6 ? 2 : 4;                    // qh offset (Q5_0, Q5_1)
+        constexpr int kQs = T == 2 ? 2 : (T == 6 ? 6 : 8);     // qs offset
+        const int h = lane & 1;
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+            const int blk = (warp * kPasses + ps) * F::BPG + (lane >> 1);
+            if (blk < nb) {
+                const int bo = blk * F::BB;              // 2-byte aligned (Q5_1: 8-byte)
+                const uint32_t d16 = lds_u16(sm, bo);
+                const uint2 w = lds8_a2(sm, bo + kQs + 8 * h);
+                uint32_t l0 = w.x & 0x0F0F0F0Fu, l1 = w.y & 0x0F0F0F0Fu;
+                uint32_t u0 = (w.x >> 4) & 0x0F0F0F0Fu, u1 = (w.y >> 4) & 0x0F0F0F0Fu;
+                if constexpr (T != 2) {
+                    const uint32_t qh = lds_u16(sm, bo + kQh) | (lds_u16(sm, bo + kQh + 2) << 16);
+                    const uint32_t lo_bits = qh >> (8 * h), hi_bits = qh >> (16 + 8 * h);
+                    l0 |= spread4_bit4(lo_bits);
+                    l1 |= spread4_bit4(lo_bits >> 4);
+                    u0 |= spread4_bit4(hi_bits);
+                    u1 |= spread4_bit4(hi_bits >> 4);
+                }
+                uint4 y0, y1;
+                if constexpr (T == 7) {
+                    // y = RN16(RN32(d * q5 + m))
+                    const float d = f16_bits_to_f32(d16), m = f16_bits_to_f32(lds_u16(sm, bo + 2));
+                    const uint64_t a2 = f32x2(d, d), m2 = f32x2(m, m);
+                    y0 = fma_bytes_eight(a2, m2, l0, l1);
+                    y1 = fma_bytes_eight(a2, m2, u0, u1);
+                } else {
+                    // y = RN16(d * (q - 8)) (Q4_0), RN16(d * (q5 - 16)) (Q5_0)
+                    constexpr uint32_t kBias = T == 2 ? 0x64086408u : 0x64106410u;   // f16 1032 / 1040
+                    y0 = f16_bias_eight(d16, l0, l1, kBias);
+                    y1 = f16_bias_eight(d16, u0, u1, kBias);
+                }
+                const uint32_t bi = static_cast<uint32_t>(b0 + blk);
+                stg_v4(dest<F::QK>(out, bi, 8 * h, mode, K, ldo, br), y0);
+                stg_v4(dest<F::QK>(out, bi, 16 + 8 * h, mode, K, ldo, br), y1);
             }
         }
     } else {
@@ -241,8 +305,12 @@ cudaError_t launch_dequant(int type, const void *q, int64_t nblocks, __half *out
     if (nblocks <= 0)
         return cudaSuccess;
     switch (type) {
+    case 2: return launch_t<2>(q, nblocks, out, K, ldo, s);
+    case 6: return launch_t<6>(q, nblocks, out, K, ldo, s);
+    case 7: return launch_t<7>(q, nblocks, out, K, ldo, s);
     case 8: return launch_t<8>(q, nblocks, out, K, ldo, s);
     case 12: return launch_t<12>(q, nblocks, out, K, ldo, s);
+    case 13: return launch_t<13>(q, nblocks, out, K, ldo, s);
     case 14: return launch_t<14>(q, nblocks, out, K, ldo, s);
     default: return cudaErrorInvalidValue;
     }

@@ -104,9 +104,92 @@ __host__ __device__ constexpr uint32_t a_col0_for(int bn)
 }
 
 template <int QT> struct QF;
-template <> struct QF<8> { static constexpr int QK = 32, BB = 34; };
-template <> struct QF<12> { static constexpr int QK = 256, BB = 144; };
-template <> struct QF<14> { static constexpr int QK = 256, BB = 210; };
+template <> struct QF<2> { static constexpr int QK = 32, BB = 18; };     // Q4_0
+template <> struct QF<6> { static constexpr int QK = 32, BB = 22; };     // Q5_0
+template <> struct QF<7> { static constexpr int QK = 32, BB = 24; };     // Q5_1
+template <> struct QF<8> { static constexpr int QK = 32, BB = 34; };     // Q8_0
+template <> struct QF<12> { static constexpr int QK = 256, BB = 144; };  // Q4_K
+template <> struct QF<13> { static constexpr int QK = 256, BB = 176; };  // Q5_K
+template <> struct QF<14> { static constexpr int QK = 256, BB = 210; };  // Q6_K
+
+// Whole 32-element blocks of Q4_0 / Q5_0 / Q5_1 at a 2-byte-aligned shared
+// address, into out[0..3] (8 f16 each, elements 0..31 in order): element e
+// is the low nibble of qs[e] (e < 16) or the high nibble of qs[e-16], with
+// bit e of the 32-bit qh plane as fifth bit for Q5_0 / Q5_1.
+template <int QT>
+__device__ __forceinline__ void small_block32(uint32_t blk, uint4 (&out)[4])
+{
+    constexpr int kQs = QT == 2 ? 2 : (QT == 6 ? 6 : 8);
+    uint32_t q[4];
+    lds_16B_a2(blk + kQs, q);
+    uint32_t v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[i] = q[i] & 0x0F0F0F0Fu;             // elements 4i .. 4i+3
+        v[4 + i] = (q[i] >> 4) & 0x0F0F0F0Fu;  // elements 16+4i .. 16+4i+3
+    }
+    if constexpr (QT != 2) {
+        constexpr int kQh = QT == 6 ? 2 : 4;
+        const uint32_t qh = lds_u16(blk + kQh) | (lds_u16(blk + kQh + 2) << 16);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            v[i] |= spread4_bit4(qh >> (4 * i));
+    }
+    const uint32_t d16 = lds_u16(blk);
+    if constexpr (QT == 7) {
+        const float d = f16_bits_to_f32(d16), m = f16_bits_to_f32(lds_u16(blk + 2));
+        const uint64_t a2 = f32x2(d, d), m2 = f32x2(m, m);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            out[i] = fma_bytes_eight(a2, m2, v[2 * i], v[2 * i + 1]);
+    } else {
+        constexpr uint32_t kBias = QT == 2 ? 0x64086408u : 0x64106410u;   // f16 1032 (q - 8) / 1040 (q - 16)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            out[i] = f16_bias_eight(d16, v[2 * i], v[2 * i + 1], kBias);
+    }
+}
+
+// Q4_K / Q5_K: (d*sc, -dmin*m) of sub-blocks 2j and 2j+1 from the block
+// header (d | dmin, scale bytes 0..3, 4..7, 8..11): the block format's
+// packing rule applied four bytes at a time, then the byte pair 2(j%2).
+__device__ __forceinline__ void kquant_pair_scales(uint4 hdr, int j, float &A0, float &A1, float &nB0, float &nB1)
+{
+    uint32_t scw, mnw;
+    if (j < 2) {
+        scw = hdr.y & 0x3F3F3F3Fu;
+        mnw = hdr.z & 0x3F3F3F3Fu;
+    } else {
+        scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+        mnw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    }
+    const int bsel = 2 * (j & 1);
+    const uint64_t m2 = f32x2(-8388608.0f, -8388608.0f);
+    const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
+    unpack_f32x2(mul_f32x2(add_f32x2(magic_pair(scw, bsel), m2), f32x2(d, d)), A0, A1);
+    unpack_f32x2(mul_f32x2(add_f32x2(magic_pair(mnw, bsel), m2), f32x2(-dmin, -dmin)), nB0, nB1);
+}
+
+// Q5_K sub-block s (elements 32s .. 32s+31) of the 16-byte-aligned block at
+// b, given that sub-block's d*sc (A) and -(dmin*m) (nB): nibble (low for
+// even s, high for odd) of qs[32(s/2) + i] plus bit s of qh[i] as fifth bit.
+__device__ __forceinline__ void q5k_sub32(uint32_t b, int s, float A, float nB, uint4 (&out)[4])
+{
+    const uint4 q0 = lds_v4(b + 48 + 32 * (s >> 1)), q1 = lds_v4(b + 64 + 32 * (s >> 1));
+    const uint4 h0 = lds_v4(b + 16), h1 = lds_v4(b + 32);
+    const int nsh = 4 * (s & 1);
+    const int hrot = (s + 28) & 31;   // rotate bit s of every byte onto bit 4
+    const uint64_t a2 = f32x2(A, A), nb2 = f32x2(nB, nB);
+    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    uint32_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] = ((qw[i] >> nsh) & 0x0F0F0F0Fu) | (__funnelshift_r(hw[i], hw[i], hrot) & 0x10101010u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        out[i] = fma_bytes_eight(a2, nb2, v[2 * i], v[2 * i + 1]);
+}
 
 struct RowSpan {
     int64_t s0;       // 16-byte-aligned start of the copied range in the stream
@@ -184,6 +267,38 @@ __device__ __forceinline__ void decode32<8>(uint32_t b, int o, uint4 (&out)[4])
         out[j] = q80_eight(d16, q[2 * j], q[2 * j + 1]);
 }
 
+template <>
+__device__ __forceinline__ void decode32<2>(uint32_t b, int o, uint4 (&out)[4])
+{
+    (void)o;   // Q4_0: one whole block (o == 0), 2-byte aligned
+    small_block32<2>(b, out);
+}
+
+template <>
+__device__ __forceinline__ void decode32<6>(uint32_t b, int o, uint4 (&out)[4])
+{
+    (void)o;   // Q5_0
+    small_block32<6>(b, out);
+}
+
+template <>
+__device__ __forceinline__ void decode32<7>(uint32_t b, int o, uint4 (&out)[4])
+{
+    (void)o;   // Q5_1
+    small_block32<7>(b, out);
+}
+
+template <>
+__device__ __forceinline__ void decode32<13>(uint32_t b, int o, uint4 (&out)[4])
+{
+    // Q5_K: b is 16-byte aligned; elements o .. o+31 are sub-block o/32.
+    const uint4 hdr = lds_v4(b);
+    const int s = o >> 5;
+    float A0, A1, nB0, nB1;
+    kquant_pair_scales(hdr, s >> 1, A0, A1, nB0, nB1);
+    q5k_sub32(b, s, (s & 1) ? A1 : A0, (s & 1) ? nB1 : nB0, out);
+}
+
 // Block-aligned weights (K % 256 == 0): one raw chunk of a row is 256
 // consecutive elements starting on a block boundary -- one Q4_K or Q6_K
 // block, or eight Q8_0 blocks -- at `b` (the row's slot plus its leading
@@ -213,22 +328,8 @@ __device__ __forceinline__ void decode_step<12>(uint32_t b, int j, uint32_t col)
     // low nibbles for sub-block 2j (half 0), high nibbles for 2j+1 (half 1).
     const uint4 hdr = lds_v4(b);   // d | dmin, scale bytes 0..3, 4..7, 8..11
     const uint4 q0 = lds_v4(b + 16 + 32 * j), q1 = lds_v4(b + 32 + 32 * j);
-    // 6-bit scales (scw) and mins (mnw) of sub-blocks 4*(j/2) .. +3, one per
-    // byte: the block format's packing rule applied four bytes at a time.
-    uint32_t scw, mnw;
-    if (j < 2) {
-        scw = hdr.y & 0x3F3F3F3Fu;
-        mnw = hdr.z & 0x3F3F3F3Fu;
-    } else {
-        scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
-        mnw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
-    }
-    const int bsel = 2 * (j & 1);   // bytes of sub-blocks 2j, 2j+1
-    const uint64_t m2 = f32x2(-8388608.0f, -8388608.0f);
-    const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
     float A0, A1, nB0, nB1;   // d*sc and -(dmin*m) of the two sub-blocks, exact
-    unpack_f32x2(mul_f32x2(add_f32x2(magic_pair(scw, bsel), m2), f32x2(d, d)), A0, A1);
-    unpack_f32x2(mul_f32x2(add_f32x2(magic_pair(mnw, bsel), m2), f32x2(-dmin, -dmin)), nB0, nB1);
+    kquant_pair_scales(hdr, j, A0, A1, nB0, nB1);
     {
         const uint64_t a2 = f32x2(A0, A0), nb2 = f32x2(nB0, nB0);
         uint4 out[4];
@@ -252,6 +353,22 @@ __device__ __forceinline__ void decode_step<12>(uint32_t b, int j, uint32_t col)
         __syncwarp();
         tmem_st_32x32b_x16(col + 16, out);
     }
+}
+
+template <>
+__device__ __forceinline__ void decode_step<13>(uint32_t b, int j, uint32_t col)
+{
+    // Q5_K, b 16-byte aligned: sub-blocks 2j (half 0) and 2j+1 (half 1).
+    const uint4 hdr = lds_v4(b);
+    float A0, A1, nB0, nB1;
+    kquant_pair_scales(hdr, j, A0, A1, nB0, nB1);
+    uint4 out[4];
+    q5k_sub32(b, 2 * j, A0, nB0, out);
+    __syncwarp();
+    tmem_st_32x32b_x16(col, out);
+    q5k_sub32(b, 2 * j + 1, A1, nB1, out);
+    __syncwarp();
+    tmem_st_32x32b_x16(col + 16, out);
 }
 
 template <>
@@ -301,6 +418,25 @@ __device__ __forceinline__ void decode_step<8>(uint32_t b, int j, uint32_t col)
         tmem_st_32x32b_x16(col + 16 * h, out);
     }
 }
+
+// Q4_0 / Q5_0 / Q5_1: a 256-element chunk is eight blocks; half h of step j
+// is the whole block 2j + h.
+#define MQ_SMALL_STEP(QT_)                                                              \
+    template <>                                                                         \
+    __device__ __forceinline__ void decode_step<QT_>(uint32_t b, int j, uint32_t col)   \
+    {                                                                                   \
+        _Pragma("unroll") for (int h = 0; h < 2; ++h)                                   \
+        {                                                                               \
+            uint4 out[4];                                                               \
+            small_block32<QT_>(b + QF<QT_>::BB * (2 * j + h), out);                     \
+            __syncwarp();                                                               \
+            tmem_st_32x32b_x16(col + 16 * h, out);                                      \
+        }                                                                               \
+    }
+MQ_SMALL_STEP(2)
+MQ_SMALL_STEP(6)
+MQ_SMALL_STEP(7)
+#undef MQ_SMALL_STEP
 
 template <int BN, int QT, bool TMA_RAW>
 __global__ void __launch_bounds__(kThreadsF, 1)
@@ -676,8 +812,28 @@ struct FusedLayout {
     int rs, x_stages, raw_stages, smem;
 };
 
-int qk_of(int qt) { return qt == 8 ? 32 : 256; }
-int bb_of(int qt) { return qt == 8 ? 34 : (qt == 12 ? 144 : 210); }
+int qk_of(int qt) { return (qt == 12 || qt == 13 || qt == 14) ? 256 : 32; }
+int bb_of(int qt)
+{
+    switch (qt) {
+    case 2: return 18;
+    case 6: return 22;
+    case 7: return 24;
+    case 8: return 34;
+    case 12: return 144;
+    case 13: return 176;
+    default: return 210;
+    }
+}
+
+// Shared-memory bytes per row of a raw stage on the tensor-map path: one
+// 256-element chunk plus the leading misalignment, rounded to 16 (only
+// Q6_K chunks start off a 16-byte boundary, by up to 14 bytes).
+int tma_rs_of(int qt)
+{
+    const int chunk = 256 / qk_of(qt) * bb_of(qt);
+    return qt == 14 ? 224 : chunk;
+}
 
 // Shared-memory plan: per-row raw slot size and the depth of the raw ring
 // within 227 KB (the f16 weight operand lives in TMEM; the activation ring
@@ -688,7 +844,7 @@ FusedLayout fused_layout(int qt, int bn, bool tma_raw)
 {
     FusedLayout L{};
     if (tma_raw) {
-        L.rs = qt == 12 ? 144 : (qt == 14 ? 224 : 272);
+        L.rs = tma_rs_of(qt);
     } else {
         // A 256-element chunk of a row whose start is a multiple of 64
         // elements touches 256/QK blocks (QK = 32) or up to 2 (QK = 256);
@@ -776,7 +932,7 @@ PFN_encodeTiledF encoder()
 
 int encode_raw_maps(RawMaps *maps, const void *qdata, int type, int64_t N, int64_t K)
 {
-    if (K % 256 != 0 || (type != 8 && type != 12 && type != 14))
+    if (K % 256 != 0 || (type != 2 && type != 6 && type != 7 && type != 8 && type != 12 && type != 13 && type != 14))
         return 0;
     PFN_encodeTiledF fn = encoder();
     if (!fn)
@@ -785,7 +941,7 @@ int encode_raw_maps(RawMaps *maps, const void *qdata, int type, int64_t N, int64
     int g = 1;
     while ((g * rb) % 16 != 0)
         g *= 2;                                   // rb is even, so g <= 8
-    const int box_bytes = type == 12 ? 144 : (type == 14 ? 224 : 272);
+    const int box_bytes = tma_rs_of(type);
     for (int c = 0; c < g; ++c) {
         const int64_t rows = (N - c + g - 1) / g;   // rows n = c, c+g, ... < N
         if (rows <= 0) {
@@ -813,7 +969,11 @@ cudaError_t launch_gemm_fused(const CUtensorMap &tx, const RawMaps &maps, const 
         return cudaErrorInvalidValue;
     const bool tma = a.raw_g > 0;
     switch (a.qtype) {
+    case 2: return tma ? launch_q<2, true>(tx, maps, a, p, s) : launch_q<2, false>(tx, maps, a, p, s);
+    case 6: return tma ? launch_q<6, true>(tx, maps, a, p, s) : launch_q<6, false>(tx, maps, a, p, s);
+    case 7: return tma ? launch_q<7, true>(tx, maps, a, p, s) : launch_q<7, false>(tx, maps, a, p, s);
     case 8: return tma ? launch_q<8, true>(tx, maps, a, p, s) : launch_q<8, false>(tx, maps, a, p, s);
+    case 13: return tma ? launch_q<13, true>(tx, maps, a, p, s) : launch_q<13, false>(tx, maps, a, p, s);
     case 12: return tma ? launch_q<12, true>(tx, maps, a, p, s) : launch_q<12, false>(tx, maps, a, p, s);
     case 14: return tma ? launch_q<14, true>(tx, maps, a, p, s) : launch_q<14, false>(tx, maps, a, p, s);
     default: return cudaErrorInvalidValue;

@@ -190,4 +190,35 @@ __device__ __forceinline__ uint4 q80_eight(uint32_t d16, uint32_t w0, uint32_t w
     return make_uint4(q80_pair(v0, 0, d2), q80_pair(v0, 2, d2), q80_pair(v1, 0, d2), q80_pair(v1, 2, d2));
 }
 
+// Eight outputs y_j = RN16(d * (c_j - bias)) from bytes c_j of (v0, v1)
+// (bytes 0..3 of v0 first): the byte permute puts c_j under the f16
+// exponent of 1024 (0x64nn = 1024 + nn), subtracting 1024 + bias (given as
+// f16x2 bits in bias2) is exact, and one f16 multiply by d rounds once.
+// d * (c_j - bias) is exact in f32 whenever |c_j - bias| < 2^13 (d has 11
+// significant bits), so this equals RN16(RN32(d * q)).
+__device__ __forceinline__ uint32_t f16_bias_pair(uint32_t v, int j, uint32_t bias2, uint32_t d2)
+{
+    const uint32_t h = __byte_perm(v, 0x64646464u, 0x5040u | j | ((j + 1) << 8));
+    uint32_t q, y;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(q) : "r"(h), "r"(bias2));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(q), "r"(d2));
+    return y;
+}
+
+__device__ __forceinline__ uint4 f16_bias_eight(uint32_t d16, uint32_t v0, uint32_t v1, uint32_t bias2)
+{
+    const uint32_t d2 = (d16 & 0xFFFFu) * 0x10001u;
+    return make_uint4(f16_bias_pair(v0, 0, bias2, d2), f16_bias_pair(v0, 2, bias2, d2),
+                      f16_bias_pair(v1, 0, bias2, d2), f16_bias_pair(v1, 2, bias2, d2));
+}
+
+// Bits 0..3 of x spread to bit 4 of bytes 0..3 (0x10 per set bit): the
+// multiply moves bit i to bit 8i, the mask keeps those, the shift lifts
+// them to bit 4.  Used for Q5_0 / Q5_1's qh bit plane (the fifth bit of
+// four consecutive elements).
+__device__ __forceinline__ uint32_t spread4_bit4(uint32_t x)
+{
+    return (((x & 0xFu) * 0x00204081u) & 0x01010101u) << 4;
+}
+
 }  // namespace mq

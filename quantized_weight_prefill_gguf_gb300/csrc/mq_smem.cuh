@@ -43,4 +43,18 @@ __device__ __forceinline__ void lds_32B_a2(uint32_t saddr, uint32_t (&w)[8])
         w[i] = __funnelshift_r(t[i], t[i + 1], sh);
 }
 
+// 16 bytes starting at a 2-byte-aligned shared address, as 4 words.
+__device__ __forceinline__ void lds_16B_a2(uint32_t saddr, uint32_t (&w)[4])
+{
+    const uint32_t base = saddr & ~3u;
+    const uint32_t sh = (saddr & 3u) * 8u;
+    uint32_t t[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+        t[i] = lds_u32(base + 4 * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w[i] = __funnelshift_r(t[i], t[i + 1], sh);
+}
+
 }  // namespace mq

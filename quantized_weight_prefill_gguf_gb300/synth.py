@@ -16,11 +16,19 @@ drawn in the listed order, then the activations):
   uniform on {-128..127}, d ~ U[2e-4, 1e-3] as f16 at byte 208.
 * Q8_0 block (34 B): d ~ U[1e-3, 5e-3] as f16 at byte 0, 32 int8 quants
   uniform on {-127..127}.
+* Q4_0 block (18 B): d ~ U[1e-3, 5e-3] as f16 at byte 0, 16 nibble bytes.
+* Q5_0 block (22 B): d ~ U[1e-3, 5e-3] as f16 at byte 0, the 4-byte qh bit
+  plane at byte 2, 16 nibble bytes at byte 6 (all uniform bytes).
+* Q5_1 block (24 B): d ~ U[5e-4, 2e-3] and m ~ U[-2e-2, 0] as f16 at bytes
+  0 and 2, qh at byte 4, 16 nibble bytes at byte 8.
+* Q5_K block (176 B): d, dmin as Q4_K at bytes 0 and 2, 12 scale/min bytes
+  at 4, 32 qh bytes at 16, 128 nibble bytes at 48 (uniform bytes).
 * Activations X[M,K] ~ N(0,1) in f32, rounded to f16.
 
 Draw order inside a weight: Q4_K d, dmin, scale bytes, nibble bytes;
-Q6_K ql, qh, scales, d; Q8_0 d, quants.  Field values are drawn for all
-blocks of the weight at once.
+Q6_K ql, qh, scales, d; Q8_0 d, quants; Q4_0 d, nibbles; Q5_0 d, qh,
+nibbles; Q5_1 d, m, qh, nibbles; Q5_K d, dmin, scale bytes, qh, nibbles.
+Field values are drawn for all blocks of the weight at once.
 """
 from __future__ import annotations
 
@@ -28,9 +36,11 @@ from dataclasses import dataclass
 
 import numpy as np
 
-Q8_0, Q4_K, Q6_K = 8, 12, 14
-BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
-TYPE_NAME = {Q8_0: "q8_0", Q4_K: "q4_K", Q6_K: "q6_K"}
+Q4_0, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 6, 7, 8, 12, 13, 14
+BLOCK = {Q4_0: (32, 18), Q5_0: (32, 22), Q5_1: (32, 24), Q8_0: (32, 34), Q4_K: (256, 144),
+         Q5_K: (256, 176), Q6_K: (256, 210)}
+TYPE_NAME = {Q4_0: "q4_0", Q5_0: "q5_0", Q5_1: "q5_1", Q8_0: "q8_0", Q4_K: "q4_K", Q5_K: "q5_K",
+             Q6_K: "q6_K"}
 
 
 def rng(seed: int = 0) -> np.random.Generator:
@@ -77,7 +87,56 @@ def q8_0_blocks(g: np.random.Generator, nblocks: int) -> np.ndarray:
     return b.reshape(-1)
 
 
-_DRAW = {Q4_K: q4_K_blocks, Q6_K: q6_K_blocks, Q8_0: q8_0_blocks}
+def q4_0_blocks(g: np.random.Generator, nblocks: int) -> np.ndarray:
+    d = g.uniform(1e-3, 5e-3, nblocks)
+    qs = g.integers(0, 256, (nblocks, 16), dtype=np.uint8)
+    b = np.empty((nblocks, 18), dtype=np.uint8)
+    b[:, 0:2] = _f16_le_bytes(d)
+    b[:, 2:18] = qs
+    return b.reshape(-1)
+
+
+def q5_0_blocks(g: np.random.Generator, nblocks: int) -> np.ndarray:
+    d = g.uniform(1e-3, 5e-3, nblocks)
+    qh = g.integers(0, 256, (nblocks, 4), dtype=np.uint8)
+    qs = g.integers(0, 256, (nblocks, 16), dtype=np.uint8)
+    b = np.empty((nblocks, 22), dtype=np.uint8)
+    b[:, 0:2] = _f16_le_bytes(d)
+    b[:, 2:6] = qh
+    b[:, 6:22] = qs
+    return b.reshape(-1)
+
+
+def q5_1_blocks(g: np.random.Generator, nblocks: int) -> np.ndarray:
+    d = g.uniform(5e-4, 2e-3, nblocks)
+    m = g.uniform(-2e-2, 0.0, nblocks)
+    qh = g.integers(0, 256, (nblocks, 4), dtype=np.uint8)
+    qs = g.integers(0, 256, (nblocks, 16), dtype=np.uint8)
+    b = np.empty((nblocks, 24), dtype=np.uint8)
+    b[:, 0:2] = _f16_le_bytes(d)
+    b[:, 2:4] = _f16_le_bytes(m)
+    b[:, 4:8] = qh
+    b[:, 8:24] = qs
+    return b.reshape(-1)
+
+
+def q5_K_blocks(g: np.random.Generator, nblocks: int) -> np.ndarray:
+    d = g.uniform(2e-4, 1e-3, nblocks)
+    dmin = g.uniform(0.0, 5e-4, nblocks)
+    scales = g.integers(0, 256, (nblocks, 12), dtype=np.uint8)
+    qh = g.integers(0, 256, (nblocks, 32), dtype=np.uint8)
+    qs = g.integers(0, 256, (nblocks, 128), dtype=np.uint8)
+    b = np.empty((nblocks, 176), dtype=np.uint8)
+    b[:, 0:2] = _f16_le_bytes(d)
+    b[:, 2:4] = _f16_le_bytes(dmin)
+    b[:, 4:16] = scales
+    b[:, 16:48] = qh
+    b[:, 48:176] = qs
+    return b.reshape(-1)
+
+
+_DRAW = {Q4_K: q4_K_blocks, Q6_K: q6_K_blocks, Q8_0: q8_0_blocks, Q4_0: q4_0_blocks, Q5_0: q5_0_blocks,
+         Q5_1: q5_1_blocks, Q5_K: q5_K_blocks}
 
 
 def nblocks(qtype: int, N: int, K: int) -> int:
@@ -115,6 +174,10 @@ LLAMA31_8B = [("q", Q4_K, 4096, 4096), ("k", Q4_K, 1024, 4096), ("v", Q4_K, 1024
               ("up", Q4_K, 14336, 4096), ("down", Q4_K, 4096, 14336)]
 Q8_0_PAIR = [("w1", Q8_0, 3584, 18944), ("w2", Q8_0, 18944, 3584)]
 SINGLE_896 = [("w", Q4_K, 896, 896)]
+# The other block formats (Q4_0 / Q5_0 / Q5_1 / Q5_K), each at the 7B gate
+# (18944 x 3584) and down (3584 x 18944) shapes.
+MORE_FORMATS = [(f"{TYPE_NAME[t]}_{nm}", t, n, k) for t in (Q4_0, Q5_0, Q5_1, Q5_K)
+                for nm, n, k in (("gate", 18944, 3584), ("down", 3584, 18944))]
 
 WORKLOADS = {
     # name: (weights, token counts M)
@@ -122,6 +185,7 @@ WORKLOADS = {
     "qwen2.5-7b_layer": (QWEN25_7B, [2048]),
     "llama3.1-8b_layer": (LLAMA31_8B, [512]),
     "q8_0_pair": (Q8_0_PAIR, [128, 1024]),
+    "more_formats": (MORE_FORMATS, [32, 2048]),
     "small_m_sweep": ([w for w in QWEN25_7B if w[0] in ("gate", "up", "down")],
                       [1, 8, 32, 128, 256, 512, 2048]),
 }

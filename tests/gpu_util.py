@@ -4,6 +4,8 @@ from __future__ import annotations
 import numpy as np
 import pytest
 
+from quantized_weight_prefill_gguf_gb300.synth import TYPE_NAME
+
 # Tolerance for GEMM outputs against the oracle's f64 result: relative
 # Frobenius error <= 1e-3 and max abs error <= 5e-3 * max|Y_ref|.  f16 x f16
 # products are exact in f32, so the kernels' only error is f32 accumulation
@@ -51,3 +53,27 @@ def sample_indices(M, N, count, seed=0):
     mi = np.concatenate([np.array([p[0] for p in pts]), g.integers(0, M, count)])
     ni = np.concatenate([np.array([p[1] for p in pts]), g.integers(0, N, count)])
     return mi.astype(np.int64), ni.astype(np.int64)
+
+
+def check_cache(orc, w, flags=0, expect_ldk=None):
+    """Registers weight w and compares its f16 cache with the oracle's
+    decode bit for bit; pad columns (ldk > K) must hold +0.0."""
+    torch = torch_cuda()
+    import quantized_weight_prefill_gguf_gb300 as mq
+    q = dev(w.data)
+    h = mq.mq_register_weight(w.qtype, q, w.N, w.K, flags=flags)
+    mq.mq_stream_status()
+    n, k, ldk, _ = h.info()
+    assert (n, k) == (w.N, w.K)
+    if expect_ldk is not None:
+        assert ldk == expect_ldk
+    cache = h.cache_tensor().cpu().numpy().view(np.uint16)
+    ref = orc.decode_matrix(w.qtype, w.data, w.N, w.K)
+    got = cache[:, : w.K]
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, (f"{TYPE_NAME[w.qtype]} {w.N}x{w.K}: {len(bad)} mismatches, first at "
+                           f"{bad[0].tolist()}: got 0x{int(got[tuple(bad[0])]):04x} want 0x{int(ref[tuple(bad[0])]):04x}")
+    if ldk > w.K:
+        assert np.all(cache[:, w.K:] == 0), "pad columns must hold +0.0"
+    h.release()
+    del torch

@@ -6,9 +6,10 @@ a mismatch.  ``test_oracle.py`` runs them against the oracle; the mutation
 test runs them against deliberately broken copies of it to show that every
 planted mistake is caught by at least one pin.
 
-Block layouts pinned here are the GGUF convention for Q8_0 / Q4_K / Q6_K;
-the pages name the types and block sizes only ("05 · 8p — Persistent f16
-weight cache + fused dequant-in-GEMM", section 1).  Hand-built blocks below
+Block layouts pinned here are the GGUF convention for Q8_0 / Q4_K / Q6_K and
+Q4_0 / Q5_0 / Q5_1 / Q5_K; the pages name the types and block sizes (and
+Q5_0's fields) only ("05 · 8p — Persistent f16 weight cache + fused
+dequant-in-GEMM", sections 1 and 2).  Hand-built blocks below
 are written byte by byte from that layout, independently of the oracle's
 decoder and of its encoders.
 """
@@ -19,7 +20,7 @@ from fractions import Fraction
 
 import numpy as np
 
-Q8_0, Q4_K, Q6_K = 8, 12, 14
+Q4_0, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 6, 7, 8, 12, 13, 14
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 ONE = 0x3C00        # f16 1.0
@@ -456,6 +457,174 @@ def pin_gemm_sampled_matches_full(orc):
     ni = g.integers(0, N, 50)
     ys = orc.gemm_f64_sampled(X, W, mi, ni)
     assert np.array_equal(ys, Y[mi, ni])
+
+
+# ---------------------------------------------------------------------------
+# O2: Q4_0 / Q5_0 / Q5_1 (32-element blocks)
+# ---------------------------------------------------------------------------
+
+def q40_bytes(d: int, qs) -> np.ndarray:
+    assert len(qs) == 16
+    return np.array(le16(d) + list(qs), dtype=np.uint8)
+
+
+def q50_bytes(d: int, qh: int, qs) -> np.ndarray:
+    assert len(qs) == 16
+    return np.array(le16(d) + [(qh >> (8 * i)) & 0xFF for i in range(4)] + list(qs), dtype=np.uint8)
+
+
+def q51_bytes(d: int, m: int, qh: int, qs) -> np.ndarray:
+    assert len(qs) == 16
+    return np.array(le16(d) + le16(m) + [(qh >> (8 * i)) & 0xFF for i in range(4)] + list(qs), dtype=np.uint8)
+
+
+def nibble_of(qs, e: int) -> int:
+    """Element e of a 32-element block: low nibble of byte e (e < 16), high
+    nibble of byte e-16."""
+    return (qs[e] & 15) if e < 16 else (qs[e - 16] >> 4)
+
+
+def pin_q4_0_values(orc):
+    """d = 1: element e decodes to its nibble - 8 (low nibbles first)."""
+    g = np.random.Generator(np.random.PCG64(21))
+    blocks, exps = [], []
+    for _ in range(32):
+        qs = g.integers(0, 256, 16).tolist()
+        blocks.append(q40_bytes(ONE, qs))
+        exps += [nibble_of(qs, e) - 8 for e in range(32)]
+    out = orc.decode(Q4_0, np.concatenate(blocks))
+    assert np.array_equal(out, ints_to_f16bits(exps))
+
+
+def pin_q4_0_sign_and_tie(orc):
+    """Nibble 8 with d = -1 gives -0; d = 1+2^-10 with nibble 11 (q = 3)
+    gives the binary16 tie 3+3*2^-10, rounded to even 0x4202."""
+    out = orc.decode(Q4_0, q40_bytes(MINUS_ONE, [0x88] * 16))
+    assert np.all(out == 0x8000)
+    out = orc.decode(Q4_0, q40_bytes(0x3C01, [0x8B] + [0x88] * 15))
+    assert int(out[0]) == 0x4202 and np.all(out[1:] == 0)
+
+
+def pin_q5_0_values(orc):
+    """d = 1: element e decodes to (nibble | bit e of qh << 4) - 16."""
+    g = np.random.Generator(np.random.PCG64(22))
+    blocks, exps = [], []
+    for _ in range(32):
+        qs = g.integers(0, 256, 16).tolist()
+        qh = int(g.integers(0, 2**32))
+        blocks.append(q50_bytes(ONE, qh, qs))
+        exps += [(nibble_of(qs, e) | (((qh >> e) & 1) << 4)) - 16 for e in range(32)]
+    out = orc.decode(Q5_0, np.concatenate(blocks))
+    assert np.array_equal(out, ints_to_f16bits(exps))
+
+
+def pin_q5_0_single_qh_bit(orc):
+    """With every nibble 0, one set bit e of qh lifts exactly element e from
+    -16 to 0 (d = 1)."""
+    blocks = [q50_bytes(ONE, 1 << e, [0] * 16) for e in range(32)]
+    out = orc.decode(Q5_0, np.concatenate(blocks)).reshape(32, 32)
+    exp = np.full((32, 32), -16)
+    np.fill_diagonal(exp, 0)
+    assert np.array_equal(out, ints_to_f16bits(exp).reshape(32, 32))
+
+
+def pin_q5_0_tie(orc):
+    """q5 = 19 (q = 3), d = 1+2^-10: the tie 3+3*2^-10 rounds to 0x4202."""
+    out = orc.decode(Q5_0, q50_bytes(0x3C01, 1, [0x03] + [0] * 15))
+    assert int(out[0]) == 0x4202, hex(int(out[0]))
+
+
+def pin_q5_1_values(orc):
+    """d = 1, m = 1/2: element e decodes to q5 + 1/2 (no offset in Q5_1)."""
+    g = np.random.Generator(np.random.PCG64(23))
+    blocks, exps = [], []
+    for _ in range(32):
+        qs = g.integers(0, 256, 16).tolist()
+        qh = int(g.integers(0, 2**32))
+        blocks.append(q51_bytes(ONE, HALF, qh, qs))
+        exps += [(nibble_of(qs, e) | (((qh >> e) & 1) << 4)) + 0.5 for e in range(32)]
+    out = orc.decode(Q5_1, np.concatenate(blocks))
+    assert np.array_equal(out, np.array(exps).astype(np.float16).view(np.uint16))
+
+
+def pin_q5_1_double_rounding(orc):
+    """d = 293/2048, q5 = 7 gives d*q = 1+3*2^-11 exactly; m = -2^-24.  The
+    binary32 sum rounds (a tie, to even) to 1+3*2^-11, a binary16 tie that
+    goes to 0x3C02; rounding the exact sum straight to binary16 would give
+    0x3C01.  q5 = 0 elements give 0*d + m = -2^-24 (0x8001)."""
+    out = orc.decode(Q5_1, q51_bytes(f16bits(293 / 2048), 0x8001, 0, [0x07] + [0] * 15))
+    assert int(out[0]) == 0x3C02, hex(int(out[0]))
+    assert np.all(out[1:] == 0x8001)
+
+
+# ---------------------------------------------------------------------------
+# O2: Q5_K
+# ---------------------------------------------------------------------------
+
+def q5k_bytes(d: int, dmin: int, S, qh, qs) -> np.ndarray:
+    assert len(S) == 12 and len(qh) == 32 and len(qs) == 128
+    return np.array(le16(d) + le16(dmin) + list(S) + list(qh) + list(qs), dtype=np.uint8)
+
+
+def pin_q5k_values(orc):
+    """d = 1, dmin = 0, every scale 1: element 64p+i is the low nibble of
+    qs[32p+i] plus 16 * bit 2p of qh[i]; element 64p+32+i the high nibble
+    plus 16 * bit 2p+1 of qh[i]."""
+    g = np.random.Generator(np.random.PCG64(24))
+    blocks, exps = [], []
+    for _ in range(16):
+        qs = g.integers(0, 256, 128).tolist()
+        qh = g.integers(0, 256, 32).tolist()
+        blocks.append(q5k_bytes(ONE, 0, S_SC1_M0, qh, qs))
+        e = [0] * 256
+        for p in range(4):
+            for i in range(32):
+                e[64 * p + i] = (qs[32 * p + i] & 15) + 16 * ((qh[i] >> (2 * p)) & 1)
+                e[64 * p + 32 + i] = (qs[32 * p + i] >> 4) + 16 * ((qh[i] >> (2 * p + 1)) & 1)
+        exps += e
+    out = orc.decode(Q5_K, np.concatenate(blocks))
+    assert np.array_equal(out, ints_to_f16bits(exps))
+
+
+def pin_q5k_single_qh_bit(orc):
+    """With all nibbles 0, bit s of qh byte i lights exactly element 32s+i
+    (sub-block s, position i) with 16."""
+    blocks, exps = [], []
+    for s in range(8):
+        for i in range(32):
+            qh = [0] * 32
+            qh[i] = 1 << s
+            blocks.append(q5k_bytes(ONE, 0, S_SC1_M0, qh, [0] * 128))
+            e = np.zeros(256, dtype=np.int64)
+            e[32 * s + i] = 16
+            exps.append(e)
+    out = orc.decode(Q5_K, np.concatenate(blocks)).reshape(256, 256)
+    assert np.array_equal(out, ints_to_f16bits(np.stack(exps)).reshape(256, 256))
+
+
+def pin_q5k_scale_bytes(orc):
+    """Random scale bytes (packed as in Q4_K), nibbles 1 and qh 0, d = 2,
+    dmin = 1/2: sub-block s decodes to 2*sc_s - m_s/2."""
+    g = np.random.Generator(np.random.PCG64(25))
+    blocks, exps = [], []
+    for _ in range(64):
+        S = g.integers(0, 256, 12).tolist()
+        blocks.append(q5k_bytes(TWO, HALF, S, [0] * 32, [0x11] * 128))
+        e = []
+        for s, (sc, m) in enumerate(q4k_expected_scale_min(S)):
+            e += [2 * sc - m / 2] * 32
+        exps.append(e)
+    out = orc.decode(Q5_K, np.concatenate(blocks)).reshape(64, 256)
+    assert np.array_equal(out, np.array(exps).astype(np.float16).view(np.uint16))
+
+
+def pin_q5k_double_rounding(orc):
+    """As for Q4_K: d*sc*q = 1+3*2^-11 (d = 293/2048, sc = 1, q = 7),
+    dmin*m = 2^-24: binary32 first gives 0x3C02, the exact value 0x3C01."""
+    S = [1, 0, 0, 0, 1, 0, 0, 0, 0, 0, 0, 0]
+    out = orc.decode(Q5_K, q5k_bytes(f16bits(293 / 2048), 0x0001, S, [0] * 32, [7] + [0] * 127))
+    assert int(out[0]) == 0x3C02, hex(int(out[0]))
+    assert np.all(out[1:32] == 0x8001) and np.all(out[32:] == 0)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

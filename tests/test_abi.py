@@ -51,8 +51,8 @@ def test_error_strings(lib):
 def test_host_validation_without_device(lib):
     """Checks that run before any device work return their codes."""
     out = ctypes.c_void_p()
-    assert lib.mq_register_weight(13, ctypes.c_void_p(16), 256, 256, 0, None, ctypes.byref(out)) == -2
-    assert b"type id 13" in lib.mq_last_error_detail()
+    assert lib.mq_register_weight(10, ctypes.c_void_p(16), 256, 256, 0, None, ctypes.byref(out)) == -2
+    assert b"type id 10" in lib.mq_last_error_detail()
     assert lib.mq_register_weight(12, None, 256, 256, 0, None, ctypes.byref(out)) == -1
     assert lib.mq_register_weight(12, ctypes.c_void_p(16), 256, 100, 0, None, ctypes.byref(out)) == -3
     assert lib.mq_register_weight(12, ctypes.c_void_p(16), 3, 264, 0, None, ctypes.byref(out)) == -3

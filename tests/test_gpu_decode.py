@@ -9,37 +9,10 @@ caller-chosen row stride.
 import numpy as np
 import pytest
 
-from gpu_util import dev, torch_cuda
+from gpu_util import check_cache, dev, torch_cuda
 from quantized_weight_prefill_gguf_gb300 import synth
 
 pytestmark = pytest.mark.gpu
-
-
-def _mq():
-    import quantized_weight_prefill_gguf_gb300 as mq
-    return mq
-
-
-def check_cache(orc, w, flags=0, expect_ldk=None):
-    torch = torch_cuda()
-    mq = _mq()
-    q = dev(w.data)
-    h = mq.mq_register_weight(w.qtype, q, w.N, w.K, flags=flags)
-    mq.mq_stream_status()
-    n, k, ldk, _ = h.info()
-    assert (n, k) == (w.N, w.K)
-    if expect_ldk is not None:
-        assert ldk == expect_ldk
-    cache = h.cache_tensor().cpu().numpy().view(np.uint16)
-    ref = orc.decode_matrix(w.qtype, w.data, w.N, w.K)
-    got = cache[:, : w.K]
-    bad = np.argwhere(got != ref)
-    assert bad.size == 0, (f"{synth.TYPE_NAME[w.qtype]} {w.N}x{w.K}: {len(bad)} mismatches, first at "
-                           f"{bad[0].tolist()}: got 0x{int(got[tuple(bad[0])]):04x} want 0x{int(ref[tuple(bad[0])]):04x}")
-    if ldk > w.K:
-        assert np.all(cache[:, w.K:] == 0), "pad columns must hold +0.0"
-    h.release()
-    del torch
 
 
 @pytest.mark.parametrize("workload", ["q4k_896", "qwen2.5-7b_layer", "llama3.1-8b_layer", "q8_0_pair"])
@@ -53,7 +26,7 @@ def test_cache_bit_exact(orc, workload):
 def test_kpad_flags(orc):
     g = synth.rng(5)
     w = synth.Weight("w", synth.Q4_K, 256, 1024, synth.weight_bytes(g, synth.Q4_K, 256, 1024))
-    mq = _mq()
+    import quantized_weight_prefill_gguf_gb300 as mq
     check_cache(orc, w, expect_ldk=1088)
     check_cache(orc, w, flags=mq.MQ_REG_NO_KPAD, expect_ldk=1024)
     w2 = synth.Weight("w", synth.Q6_K, 64, 768, synth.weight_bytes(g, synth.Q6_K, 64, 768))
@@ -74,7 +47,7 @@ def test_ragged_streams(orc, qtype, N, K):
 
 def test_dequantize_row_stride(orc):
     torch = torch_cuda()
-    mq = _mq()
+    import quantized_weight_prefill_gguf_gb300 as mq
     g = synth.rng(9)
     N, K, ldo = 96, 1280, 1352
     for qtype in (synth.Q4_K, synth.Q6_K, synth.Q8_0):

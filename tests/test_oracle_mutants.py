@@ -37,6 +37,20 @@ MUTANTS = {
     "q6k_offset": ("int q6 = (lo | (hb << 4)) - 32;", "int q6 = (lo | (hb << 4)) - 31;"),
     "q6k_unsigned_scale": ("const int8_t *sc = (const int8_t *)(b + 192);",
                            "const uint8_t *sc = (const uint8_t *)(b + 192);"),
+    "q4_0_offset": ("y[e] = oracle_f32_to_f16(d * (float)(nib - 8));", "y[e] = oracle_f32_to_f16(d * (float)(nib - 7));"),
+    "q4_0_nibble_halves": ("int nib = e < 16 ? (qs[e] & 15) : (qs[e - 16] >> 4);\n        y[e]",
+                           "int nib = e < 16 ? (qs[e] >> 4) : (qs[e - 16] & 15);\n        y[e]"),
+    "q5_qh_bit_order": ("return nib | (int)(((h >> e) & 1u) << 4);", "return nib | (int)(((h >> (e ^ 16)) & 1u) << 4);"),
+    "q5_qh_big_endian": ("uint32_t h = (uint32_t)qh[0] | ((uint32_t)qh[1] << 8) | ((uint32_t)qh[2] << 16) | ((uint32_t)qh[3] << 24);",
+                         "uint32_t h = (uint32_t)qh[3] | ((uint32_t)qh[2] << 8) | ((uint32_t)qh[1] << 16) | ((uint32_t)qh[0] << 24);"),
+    "q5_0_offset": ("(q5_value(b + 2, b + 6, e) - 16)", "(q5_value(b + 2, b + 6, e) - 15)"),
+    "q5_1_min_dropped": ("y[e] = oracle_f32_to_f16(dq + m);", "y[e] = oracle_f32_to_f16(dq);"),
+    "q5_1_offset_kept": ("float dq = d * (float)q5_value(b + 4, b + 8, e);", "float dq = d * (float)(q5_value(b + 4, b + 8, e) - 16);"),
+    "q5_1_min_scaled_by_d": ("y[e] = oracle_f32_to_f16(dq + m);", "y[e] = oracle_f32_to_f16(dq + d * m);"),
+    "q5k_qh_bit": ("int q5 = nib | (((qh[pos] >> sub) & 1) << 4);", "int q5 = nib | (((qh[pos] >> grp) & 1) << 4);"),
+    "q5k_qh_offset": ("const uint8_t *qh = b + 16;\n    const uint8_t *qs = b + 48;", "const uint8_t *qh = b + 48;\n    const uint8_t *qs = b + 16;"),
+    "q5k_wrong_subblock": ("q4k_scale_min(S, sub, &scale, &mn);", "q4k_scale_min(S, grp, &scale, &mn);"),
+    "q5k_min_dropped": ("y[e] = oracle_f32_to_f16(prod - off);", "y[e] = oracle_f32_to_f16(prod);"),
     "gemm_reversed_operand": ("acc += x[k] * w[k];", "acc += x[k] * w[K - 1 - k];"),
     "gemm_f32_accumulator": ("double acc = 0.0;", "float acc = 0.0f;"),
     "gemm_drops_last_term": ("for (int64_t k = 0; k < K; k++)\n        acc += x[k] * w[k];",
