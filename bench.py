@@ -18,10 +18,12 @@ Printed: one JSON line (rank 0) with the contract keys plus
   e2e           the same metric with host buffers: pinned-host inputs copied
                 in and all outputs copied out inside the timed region;
   decode        the one-time decoders (registration, cold) against HBM bandwidth;
-  decode_steady the decoders back to back on the 7B gate/down shapes and a
-                Q8_0 weight of the gate's shape (HBM GB/s, fraction of peak);
+  decode_steady the decoders back to back on the 7B gate/down shapes and
+                weights of the other formats at the gate's shape (HBM GB/s);
   small_m       fused vs cached over the small-M sweep, back to back over
-                rotating weight copies (crossover, HBM GB/s).
+                rotating weight copies (crossover, HBM GB/s);
+  more_formats  Q4_0 / Q5_0 / Q5_1 / Q5_K at the 7B gate and down shapes:
+                fused and cached at M = 32 and 2048, same method.
 
 --impl reference times the CPU oracle itself as the reference arm.
 """
@@ -381,6 +383,7 @@ def main():
         out["e2e"] = e2e_run(mq, torch, weights, handles, xs, ys, stream, min(args.steps, 50), flops_step, dist)
         out["small_m"] = small_m_sweep(mq, torch, stream, P)
         out["decode_steady"] = decode_steady(mq, torch, stream, P)
+        out["more_formats"] = more_formats(mq, torch, stream, P)
     if rank == 0 and world == 1 and not args.no_extras:
         tf, tokens, secs, dsec, threads = oracle_cpu_run(weights, xs, args.cpu_seconds)
         out["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -491,41 +494,49 @@ def _rotating_time_us(torch, fns, stream, reps=5):
     return statistics.median(ts)
 
 
+def _fused_vs_cached(mq, torch, stream, P, w, x_all, ms):
+    """Rows {name, M, copies, <path>_us/_tflops/_gbs/_frac_hbm} for weight w
+    at each M: per-call time of calls issued back to back over R registered
+    copies of the weight, R chosen so the weights touched (raw blocks for
+    fused, f16 caches for cached) exceed 400 MB, three times the L2: every
+    call streams its weight from HBM, as in a layer stack, and the launch gap
+    between calls is included."""
+    raw_bytes = synth.nblocks(w.qtype, w.N, w.K) * synth.BLOCK[w.qtype][1]
+    R = max(3, -(-(400 << 20) // raw_bytes))
+    qs = [torch.from_numpy(w.data).cuda() for _ in range(R)]
+    hs = [mq.mq_register_weight(w.qtype, q, w.N, w.K) for q in qs]
+    rows = []
+    for M in ms:
+        x = x_all[:M].contiguous()
+        y = torch.empty((M, w.N), dtype=torch.float32, device="cuda")
+        row = {"name": w.name, "M": M, "copies": R}
+        for path, fn in (("fused", mq.mq_gemm_fused), ("cached", mq.mq_gemm)):
+            calls = [functools.partial(fn, x, h, y, M, stream) for h in hs]
+            t_us = _rotating_time_us(torch, calls, stream)
+            wbytes = raw_bytes if path == "fused" else 2 * w.N * w.K
+            byts = wbytes + 2 * M * w.K + 4 * M * w.N
+            row[path + "_us"] = t_us
+            row[path + "_tflops"] = 2.0 * M * w.N * w.K / (t_us * 1e-6) / 1e12
+            row[path + "_gbs"] = byts / (t_us * 1e-6) / 1e9
+            row[path + "_frac_hbm"] = row[path + "_gbs"] / P["hbm_gbs"]
+        rows.append(row)
+    mq.mq_stream_status()
+    for h in hs:
+        h.release()
+    del qs
+    return rows
+
+
 def small_m_sweep(mq, torch, stream, P):
     """Fused vs cached on the 7B gate (Q4_K 18944x3584) and down (Q6_K
-    3584x18944) shapes over the M sweep.  Each point is the per-call time of
-    calls issued back to back over R registered copies of the weight, R chosen
-    so the weights touched (raw blocks for fused, f16 caches for cached) exceed
-    400 MB, three times the L2: every call streams its weight from HBM, as in
-    a layer stack, and the launch gap between calls is included."""
+    3584x18944) shapes over the M sweep (rotating weight copies)."""
     weights, xs = synth.workload("small_m_sweep", seed=0)
     res = []
     for w in weights:
         if w.name == "up":
             continue
-        raw_bytes = synth.nblocks(w.qtype, w.N, w.K) * synth.BLOCK[w.qtype][1]
-        R = max(3, -(-(400 << 20) // raw_bytes))
-        qs = [torch.from_numpy(w.data).cuda() for _ in range(R)]
-        hs = [mq.mq_register_weight(w.qtype, q, w.N, w.K) for q in qs]
         x_all = torch.from_numpy(xs[w.K]).cuda()
-        for M in synth.WORKLOADS["small_m_sweep"][1]:
-            x = x_all[:M].contiguous()
-            y = torch.empty((M, w.N), dtype=torch.float32, device="cuda")
-            row = {"name": w.name, "M": M, "copies": R}
-            for path, fn in (("fused", mq.mq_gemm_fused), ("cached", mq.mq_gemm)):
-                calls = [functools.partial(fn, x, h, y, M, stream) for h in hs]
-                t_us = _rotating_time_us(torch, calls, stream)
-                wbytes = raw_bytes if path == "fused" else 2 * w.N * w.K
-                byts = wbytes + 2 * M * w.K + 4 * M * w.N
-                row[path + "_us"] = t_us
-                row[path + "_tflops"] = 2.0 * M * w.N * w.K / (t_us * 1e-6) / 1e12
-                row[path + "_gbs"] = byts / (t_us * 1e-6) / 1e9
-                row[path + "_frac_hbm"] = row[path + "_gbs"] / P["hbm_gbs"]
-            res.append(row)
-        mq.mq_stream_status()
-        for h in hs:
-            h.release()
-        del qs
+        res += _fused_vs_cached(mq, torch, stream, P, w, x_all, synth.WORKLOADS["small_m_sweep"][1])
     cross = {}
     for name in ("gate", "down"):
         ms_ = [r["M"] for r in res if r["name"] == name and r["cached_us"] <= r["fused_us"]]
@@ -534,13 +545,27 @@ def small_m_sweep(mq, torch, stream, P):
             "method": "back to back over rotating weight copies (> 3x L2), per-call average including launch gaps"}
 
 
+def more_formats(mq, torch, stream, P):
+    """Q4_0 / Q5_0 / Q5_1 / Q5_K weights at the 7B gate (18944x3584) and down
+    (3584x18944) shapes, fused and cached at M = 32 and 2048 (rotating
+    weight copies, as for the small-M sweep)."""
+    weights, xs = synth.workload("more_formats", seed=0)
+    res = []
+    for w in weights:
+        x_all = torch.from_numpy(xs[w.K]).cuda()
+        res += _fused_vs_cached(mq, torch, stream, P, w, x_all, synth.WORKLOADS["more_formats"][1])
+    return {"rows": res, "method": "back to back over rotating weight copies (> 3x L2), per-call average"}
+
+
 def decode_steady(mq, torch, stream, P):
     """Standalone decoders (mq_dequantize) on the 7B gate (Q4_K), down (Q6_K)
-    and an 18944x3584 Q8_0 weight: per-call time of back-to-back calls over
+    and 18944x3584 weights of the other formats: per-call time of back-to-back calls over
     three input copies into one f16 output (output 136 MB, larger than L2)."""
     g = synth.rng(7)
     out = {}
-    for qt, N, K in ((synth.Q4_K, 18944, 3584), (synth.Q6_K, 3584, 18944), (synth.Q8_0, 18944, 3584)):
+    shapes = [(synth.Q4_K, 18944, 3584), (synth.Q6_K, 3584, 18944)]
+    shapes += [(qt, 18944, 3584) for qt in (synth.Q8_0, synth.Q4_0, synth.Q5_0, synth.Q5_1, synth.Q5_K)]
+    for qt, N, K in shapes:
         data = synth.weight_bytes(g, qt, N, K)
         qs = [torch.from_numpy(data).cuda() for _ in range(3)]
         dst = torch.empty((N, K), dtype=torch.float16, device="cuda")

@@ -826,13 +826,27 @@ int bb_of(int qt)
     }
 }
 
-// Shared-memory bytes per row of a raw stage on the tensor-map path: one
-// 256-element chunk plus the leading misalignment, rounded to 16 (only
-// Q6_K chunks start off a 16-byte boundary, by up to 14 bytes).
+// Row pitch of a raw stage: at least `bytes`, an odd multiple of 16.  The
+// 32 lanes of a decoder warp read the same offset of 32 consecutive slot
+// rows; an odd number of 16-byte units per row puts the 8 lanes of each
+// 16-byte load phase on 8 distinct bank quads (no conflict) and spreads
+// 4-byte loads over 8 banks (4-way at worst).  An even count can put a
+// whole warp on 2 banks (a 192-byte pitch: 16-way).
+int odd16(int bytes)
+{
+    const int u = (bytes + 15) / 16;
+    return 16 * (u | 1);
+}
+
+// Bytes per row of a raw stage on the tensor-map path (the box width): one
+// 256-element chunk plus the leading misalignment (only Q6_K chunks start
+// off a 16-byte boundary, by up to 14 bytes), padded to an odd multiple of
+// 16.  Box bytes past the chunk are the row's next bytes or the map's zero
+// fill, and are not decoded.
 int tma_rs_of(int qt)
 {
     const int chunk = 256 / qk_of(qt) * bb_of(qt);
-    return qt == 14 ? 224 : chunk;
+    return odd16(chunk + (qt == 14 ? 14 : 0));
 }
 
 // Shared-memory plan: per-row raw slot size and the depth of the raw ring
@@ -851,7 +865,7 @@ FusedLayout fused_layout(int qt, int bn, bool tma_raw)
         // the first block may sit up to 14 bytes into its 16-byte line.
         const int span = (qk_of(qt) == 32) ? 8 : 2;
         const int mis = (bb_of(qt) % 16 == 0) ? 0 : 14;
-        L.rs = (span * bb_of(qt) + mis + 15) / 16 * 16;
+        L.rs = odd16(span * bb_of(qt) + mis);
     }
     const int xb = kChunkSteps * bn * kBK * 2;   // one chunk of activations
     const int raw = kTileRows * L.rs;
