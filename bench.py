@@ -23,7 +23,12 @@ Printed: one JSON line (rank 0) with the contract keys plus
   small_m       fused vs cached over the small-M sweep, back to back over
                 rotating weight copies (crossover, HBM GB/s);
   more_formats  Q4_0 / Q5_0 / Q5_1 / Q5_K at the 7B gate and down shapes:
-                fused and cached at M = 32 and 2048, same method.
+                fused and cached at M = 32 and 2048, same method;
+  triangle      the 7B layer's seven GEMMs one call each through the cached
+                path, the per-call scratch mode and the fused path at M = 32
+                and 2048: time per layer and device bytes each mode holds;
+  row_pad       F16 / BF16 weights of the Llama-3.1-8B layer's shapes at
+                M = 512, cached GEMM on the row-padded copy vs unpadded rows.
 
 --impl reference times the CPU oracle itself as the reference arm.
 """
@@ -384,6 +389,8 @@ def main():
         out["small_m"] = small_m_sweep(mq, torch, stream, P)
         out["decode_steady"] = decode_steady(mq, torch, stream, P)
         out["more_formats"] = more_formats(mq, torch, stream, P)
+        out["triangle"] = triangle(mq, torch, stream, weights, handles, qdev, xdev)
+        out["row_pad"] = row_pad(mq, torch, stream)
     if rank == 0 and world == 1 and not args.no_extras:
         tf, tokens, secs, dsec, threads = oracle_cpu_run(weights, xs, args.cpu_seconds)
         out["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -555,6 +562,71 @@ def more_formats(mq, torch, stream, P):
         x_all = torch.from_numpy(xs[w.K]).cuda()
         res += _fused_vs_cached(mq, torch, stream, P, w, x_all, synth.WORKLOADS["more_formats"][1])
     return {"rows": res, "method": "back to back over rotating weight copies (> 3x L2), per-call average"}
+
+
+def triangle(mq, torch, stream, weights, handles, qdev, xs):
+    """The pages' time-vs-memory triangle on the 7B layer: each of the seven
+    GEMMs as its own call (no grouping) through the cached path (resident
+    f16 caches), the per-call scratch mode (one f16 scratch as large as the
+    largest weight, re-decoded every call) and the fused path (raw blocks
+    only).  Time per layer = the seven calls back to back, median of 5."""
+    fused_h = [mq.mq_register_weight(w.qtype, q, w.N, w.K, flags=mq.MQ_REG_NO_CACHE)
+               for w, q in zip(weights, qdev)]
+    scratch_elems = max(w.N * h.info()[2] for w, h in zip(weights, handles))
+    scratch = torch.empty(scratch_elems, dtype=torch.float16, device="cuda")
+    cache_bytes = sum(2 * w.N * h.info()[2] for w, h in zip(weights, handles))
+    raw_bytes = sum(w.data.size for w in weights)
+    rows = []
+    for M in (32, 2048):
+        ys = [torch.empty((M, w.N), dtype=torch.float32, device="cuda") for w in weights]
+        xm = {K: x[:M].contiguous() for K, x in xs.items()}
+        modes = {
+            "cached": [functools.partial(mq.mq_gemm, xm[w.K], h, y, M, stream)
+                       for w, h, y in zip(weights, handles, ys)],
+            "scratch": [functools.partial(mq.mq_gemm_scratch, xm[w.K], h, y, scratch, M, stream)
+                        for w, h, y in zip(weights, handles, ys)],
+            "fused": [functools.partial(mq.mq_gemm_fused, xm[w.K], h, y, M, stream)
+                      for w, h, y in zip(weights, fused_h, ys)],
+        }
+        row = {"M": M}
+        for name, calls in modes.items():
+            row[name + "_us_per_layer"] = _rotating_time_us(torch, calls, stream) * len(calls)
+        rows.append(row)
+    mq.mq_stream_status()
+    for h in fused_h:
+        h.release()
+    return {"rows": rows, "device_bytes": {"cached": raw_bytes + cache_bytes,
+                                           "scratch": raw_bytes + 2 * scratch_elems, "fused": raw_bytes},
+            "method": "seven single calls back to back (layer weights 148 MB raw / 466 MB f16, > L2)"}
+
+
+def row_pad(mq, torch, stream):
+    """Cached GEMM at M = 512 on F16 / BF16 weights of the Llama-3.1-8B
+    layer's shapes, rows padded by 128 bytes (the default for K = 4096 and
+    14336) vs unpadded (MQ_REG_NO_KPAD), back to back over R registered
+    copies (> 400 MB of weights touched)."""
+    weights, xs = synth.workload("float_layer", seed=0)
+    M = 512
+    res = []
+    for w in weights:
+        x = torch.from_numpy(xs[w.K][:M]).cuda()
+        y = torch.empty((M, w.N), dtype=torch.float32, device="cuda")
+        R = max(3, -(-(400 << 20) // (2 * w.N * w.K)))
+        qs = [torch.from_numpy(w.data).cuda() for _ in range(R)]
+        row = {"name": w.name, "M": M, "copies": R}
+        for label, flags in (("padded", 0), ("unpadded", mq.MQ_REG_NO_KPAD)):
+            hs = [mq.mq_register_weight(w.qtype, q, w.N, w.K, flags=flags) for q in qs]
+            t_us = _rotating_time_us(torch, [functools.partial(mq.mq_gemm, x, h, y, M, stream) for h in hs], stream)
+            row[label + "_us"] = t_us
+            row[label + "_tflops"] = 2.0 * M * w.N * w.K / (t_us * 1e-6) / 1e12
+            row[label + "_ldk"] = hs[0].info()[2]
+            for h in hs:
+                h.release()
+        res.append(row)
+        del qs
+    mq.mq_stream_status()
+    return {"rows": res, "method": "back to back over R registered copies, each from its own weight buffer "
+                                   "(an unpadded F16 weight is read in place)"}
 
 
 def decode_steady(mq, torch, stream, P):

@@ -44,11 +44,16 @@
 extern "C" {
 #endif
 
-/* GGUF type ids of the supported block formats.  The pages name the types;
+/* GGUF type ids of the supported weight types.  The pages name the types;
  * field layouts are the GGUF convention ("05 · 8p — Persistent f16 weight
  * cache + fused dequant-in-GEMM", sections 1-2 give Q5_0's fields and the
- * block sizes). */
+ * block sizes).  The float types are the ones whose rows "ggml-cuda: GEMM
+ * weight row padding + one-time K-padded f16 dequant for prefill", Summary,
+ * pads (F16 / BF16 / F32): a block of one element, its f16 value the
+ * element rounded to nearest even (a NaN stays a NaN, payload not kept). */
 typedef enum {
+    MQ_TYPE_F32 = 0,    /* 4-byte IEEE binary32, row-major [N, K]                     */
+    MQ_TYPE_F16 = 1,    /* 2-byte IEEE binary16, row-major [N, K]                     */
     MQ_TYPE_Q4_0 = 2,   /* 32 elements in 18 bytes: f16 d, 16 B of 4-bit quants (q - 8) */
     MQ_TYPE_Q5_0 = 6,   /* 32 elements in 22 bytes: f16 d, 4 B fifth-bit plane, 16 B of
                            low 4 bits (q - 16); 2-byte aligned blocks                   */
@@ -59,14 +64,15 @@ typedef enum {
                            scales/mins, 128 B of 4-bit quants                          */
     MQ_TYPE_Q5_K = 13,  /* 256 elements in 176 bytes: as Q4_K plus 32 B of fifth bits
                            (bit s of byte i belongs to sub-block s, position i)        */
-    MQ_TYPE_Q6_K = 14   /* 256 elements in 210 bytes: 128 B low nibbles, 64 B high
+    MQ_TYPE_Q6_K = 14,  /* 256 elements in 210 bytes: 128 B low nibbles, 64 B high
                            2-bit fields, 16 int8 scales, f16 d                          */
+    MQ_TYPE_BF16 = 30   /* 2-byte bfloat16 (the top half of a binary32), [N, K]      */
 } mq_type;
 
 /* Status codes. */
 #define MQ_OK                    0
 #define MQ_ERR_INVALID          -1  /* null pointer, unknown or released handle, bad flag  */
-#define MQ_ERR_UNSUPPORTED_TYPE -2  /* type id is not one of the mq_type block formats      */
+#define MQ_ERR_UNSUPPORTED_TYPE -2  /* type id is not one of the mq_type weight types       */
 #define MQ_ERR_SHAPE            -3  /* a size precondition does not hold                   */
 #define MQ_ERR_ALIGN            -4  /* a pointer is not 16-byte aligned                    */
 #define MQ_ERR_NO_CACHE         -5  /* mq_gemm on a handle registered with MQ_REG_NO_CACHE */
@@ -109,6 +115,15 @@ typedef struct mq_weight *mq_handle;
  * Cache layout: f16 [N, ldk] row-major, ldk = K + 64 if (2K) % 2048 == 0
  * (K % 1024 == 0) else K; the pad columns hold +0.0.  The cache is
  * library-owned and freed by mq_release_weight().
+ *
+ * Float weights (F32 / F16 / BF16; qdata is then the row-major [N, K]
+ * matrix): the cache is the weight converted to f16 with the same row
+ * padding.  An F16 weight whose rows need no padding (ldk == K, or
+ * MQ_REG_NO_KPAD, or MQ_REG_NO_CACHE) is read in place: no copy is made,
+ * mq_weight_info() returns qdata as the cache, and release frees nothing.
+ * F32 and BF16 always get the f16 copy (MQ_REG_NO_CACHE is MQ_ERR_INVALID).
+ * mq_gemm_fused() on a float weight runs the cached GEMM (there is nothing
+ * to decode on chip).
  * Errors: MQ_ERR_UNSUPPORTED_TYPE, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_INVALID,
  * MQ_ERR_OOM (nothing is left allocated), MQ_ERR_CUDA.
  */
@@ -198,6 +213,28 @@ int mq_gemm_grouped(const void *x, const mq_handle *w, int count, float *const *
  * the fused path is faster up to M = 128 and the cached path from M = 256.
  */
 int mq_gemm_auto(const void *x, mq_handle w, float *y, int64_t M, void *stream);
+
+/*
+ * mq_gemm_scratch -- per-call dequant: decode the weight's raw blocks into
+ * the caller's f16 scratch, then run the cached GEMM on it, both on
+ * `stream`.  Same Y as mq_gemm (the scratch holds the values the cache
+ * would).  Works on any handle, with or without a cache.
+ * Passage: "05 · 8p", the time-vs-memory triangle and its per-call mode
+ * (the weight is re-dequantized into an f16 scratch on every call and the
+ * GEMM reads the scratch; it saves the resident copy and costs one decode
+ * pass per call).
+ *
+ *  scratch        device memory, 16-byte aligned, caller-owned, at least
+ *                 2*N*ldk bytes (ldk from mq_weight_info); its contents on
+ *                 return are the decoded weight in the cache layout (pad
+ *                 columns not written).  Calls that overlap on the device
+ *                 must not share one scratch.
+ *  scratch_bytes  its size.
+ * Errors: as mq_gemm (minus MQ_ERR_NO_CACHE), MQ_ERR_INVALID (scratch NULL),
+ * MQ_ERR_ALIGN, MQ_ERR_SHAPE (scratch_bytes < 2*N*ldk).
+ */
+int mq_gemm_scratch(const void *x, mq_handle w, float *y, int64_t M, void *scratch,
+                    int64_t scratch_bytes, void *stream);
 
 /*
  * mq_gemm_noalloc -- the cached GEMM (same result as mq_gemm, same

@@ -22,8 +22,9 @@ SOURCES = ("oracle.c", "encode.c")
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-shared", "-fPIC"]
 
 # GGUF type ids and (elements per block, bytes per block).
+F32, F16, BF16 = 0, 1, 30
 Q4_0, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 6, 7, 8, 12, 13, 14
-BLOCK = {Q4_0: (32, 18), Q5_0: (32, 22), Q5_1: (32, 24), Q8_0: (32, 34), Q4_K: (256, 144),
+BLOCK = {F32: (1, 4), F16: (1, 2), BF16: (1, 2), Q4_0: (32, 18), Q5_0: (32, 22), Q5_1: (32, 24), Q8_0: (32, 34), Q4_K: (256, 144),
          Q5_K: (256, 176), Q6_K: (256, 210)}
 
 

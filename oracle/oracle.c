@@ -29,6 +29,13 @@
  *      The weight is one flat stream of N*K elements in consecutive blocks;
  *      element (n,k) is flat index n*K+k, so a row may start inside a block.
  *
+ *  O2f Float weights F32 / F16 / BF16 (GGUF ids 0 / 1 / 30), the types whose
+ *      rows "ggml-cuda: GEMM weight row padding + one-time K-padded f16
+ *      dequant for prefill" pads (Summary): one element per "block" (4 / 2
+ *      / 2 bytes, little-endian), y = RN16(value).  An F16 element is its
+ *      own value; a BF16 element is the upper half of a binary32 whose lower
+ *      half is zero, widened exactly and then rounded as an F32 element is.
+ *
  *  O4  GEMM with f64 accumulation in k order: Y[m,n] = sum_k X[m,k]*W[n,k]
  *      for f16 X and the f16 dequantized W, the product the pages check
  *      their kernels against ("Eager GPU Offload Without A Compute Graph",
@@ -117,7 +124,8 @@ uint16_t oracle_f32_to_f16(float f)
 /* O2: block decoders                                                 */
 /* ------------------------------------------------------------------ */
 
-enum { T_Q4_0 = 2, T_Q5_0 = 6, T_Q5_1 = 7, T_Q8_0 = 8, T_Q4_K = 12, T_Q5_K = 13, T_Q6_K = 14 };
+enum { T_F32 = 0, T_F16 = 1, T_Q4_0 = 2, T_Q5_0 = 6, T_Q5_1 = 7, T_Q8_0 = 8, T_Q4_K = 12, T_Q5_K = 13,
+       T_Q6_K = 14, T_BF16 = 30 };
 
 static uint16_t rd_u16le(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
 
@@ -280,10 +288,30 @@ static void decode_q5_K_block(const uint8_t *b, uint16_t *y)
     }
 }
 
+/* O2f: one float element -> binary16 bits. */
+static uint16_t decode_f32_elem(const uint8_t *b)
+{
+    uint32_t x = (uint32_t)b[0] | ((uint32_t)b[1] << 8) | ((uint32_t)b[2] << 16) | ((uint32_t)b[3] << 24);
+    float f;
+    memcpy(&f, &x, 4);
+    return oracle_f32_to_f16(f);
+}
+
+static uint16_t decode_bf16_elem(const uint8_t *b)
+{
+    uint32_t x = (uint32_t)rd_u16le(b) << 16;
+    float f;
+    memcpy(&f, &x, 4);
+    return oracle_f32_to_f16(f);
+}
+
 /* Elements per block (QK) and bytes per block for a GGUF type id. */
 int oracle_block_size(int type, int *qk, int *bytes)
 {
     switch (type) {
+    case T_F32:  *qk = 1;   *bytes = 4;   return 0;
+    case T_F16:  *qk = 1;   *bytes = 2;   return 0;
+    case T_BF16: *qk = 1;   *bytes = 2;   return 0;
     case T_Q4_0: *qk = 32;  *bytes = 18;  return 0;
     case T_Q5_0: *qk = 32;  *bytes = 22;  return 0;
     case T_Q5_1: *qk = 32;  *bytes = 24;  return 0;
@@ -308,6 +336,9 @@ int oracle_decode(int type, const uint8_t *q, int64_t nblocks, uint16_t *out)
         const uint8_t *b = q + i * bb;
         uint16_t *y = out + i * qk;
         switch (type) {
+        case T_F32:  y[0] = decode_f32_elem(b); break;
+        case T_F16:  y[0] = rd_u16le(b); break;
+        case T_BF16: y[0] = decode_bf16_elem(b); break;
         case T_Q4_0: decode_q4_0_block(b, y); break;
         case T_Q5_0: decode_q5_0_block(b, y); break;
         case T_Q5_1: decode_q5_1_block(b, y); break;

@@ -16,7 +16,9 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmq.so")
 
-MQ_TYPE_Q8_0, MQ_TYPE_Q4_K, MQ_TYPE_Q6_K = 8, 12, 14
+MQ_TYPE_F32, MQ_TYPE_F16, MQ_TYPE_BF16 = 0, 1, 30
+MQ_TYPE_Q4_0, MQ_TYPE_Q5_0, MQ_TYPE_Q5_1, MQ_TYPE_Q8_0 = 2, 6, 7, 8
+MQ_TYPE_Q4_K, MQ_TYPE_Q5_K, MQ_TYPE_Q6_K = 12, 13, 14
 MQ_REG_NO_CACHE, MQ_REG_NO_KPAD, MQ_REG_KPAD = 0x1, 0x2, 0x4
 STATUS = {0: "MQ_OK", -1: "MQ_ERR_INVALID", -2: "MQ_ERR_UNSUPPORTED_TYPE", -3: "MQ_ERR_SHAPE",
           -4: "MQ_ERR_ALIGN", -5: "MQ_ERR_NO_CACHE", -6: "MQ_ERR_OOM", -7: "MQ_ERR_CUDA",
@@ -25,7 +27,8 @@ STATUS = {0: "MQ_OK", -1: "MQ_ERR_INVALID", -2: "MQ_ERR_UNSUPPORTED_TYPE", -3: "
 EXPORTS = ("mq_register_weight", "mq_release_weight", "mq_weight_info", "mq_dequantize", "mq_gemm",
            "mq_gemm_fused", "mq_gemm_auto", "mq_get_m_gate", "mq_set_m_gate", "mq_reserve_workspace",
            "mq_stream_status", "mq_launch_count", "mq_error_string", "mq_last_error_detail", "mq_version",
-           "mq_trace_enable", "mq_trace_count", "mq_trace_read", "mq_gemm_noalloc", "mq_gemm_grouped")
+           "mq_trace_enable", "mq_trace_count", "mq_trace_read", "mq_gemm_noalloc", "mq_gemm_grouped",
+           "mq_gemm_scratch")
 MQ_TRACE_GEMM_CACHED, MQ_TRACE_GEMM_FUSED, MQ_TRACE_DECODE = 1, 2, 3
 
 
@@ -52,6 +55,7 @@ def _load() -> ctypes.CDLL:
         "mq_gemm_fused": ([_P, _P, _P, _I64, _P], ctypes.c_int),
         "mq_gemm_auto": ([_P, _P, _P, _I64, _P], ctypes.c_int),
         "mq_gemm_noalloc": ([_P, _P, _P, _I64, _P], ctypes.c_int),
+        "mq_gemm_scratch": ([_P, _P, _P, _I64, _P, _I64, _P], ctypes.c_int),
         "mq_gemm_grouped": ([_P, ctypes.POINTER(_P), ctypes.c_int, ctypes.POINTER(_P), _I64, _P], ctypes.c_int),
         "mq_get_m_gate": ([], _I64),
         "mq_set_m_gate": ([_I64], ctypes.c_int),
@@ -205,6 +209,14 @@ def mq_gemm_grouped(x, ws, ys, M: int | None = None, stream=None) -> None:
 def mq_gemm_noalloc(x, w: Weight, y, M: int | None = None, stream=None) -> None:
     _check(_lib().mq_gemm_noalloc(_ptr(x), w.handle, _ptr(y), M if M is not None else x.shape[0],
                                   _stream(stream)), "mq_gemm_noalloc")
+
+
+def mq_gemm_scratch(x, w: Weight, y, scratch, M: int | None = None, stream=None) -> None:
+    """Per-call dequant into `scratch` (a CUDA tensor of at least 2*N*ldk
+    bytes), then the cached GEMM on it."""
+    nbytes = scratch.numel() * scratch.element_size()
+    _check(_lib().mq_gemm_scratch(_ptr(x), w.handle, _ptr(y), M if M is not None else x.shape[0], _ptr(scratch),
+                                  nbytes, _stream(stream)), "mq_gemm_scratch")
 
 
 def mq_get_m_gate() -> int:

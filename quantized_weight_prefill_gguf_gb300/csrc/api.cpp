@@ -29,6 +29,7 @@ struct mq_weight {
     int qk, bb;
     const uint8_t *qdata;
     __half *cache;       // null when registered with MQ_REG_NO_CACHE
+    bool cache_owned;    // false: cache is the caller's F16 weight itself
     int device;
     CUtensorMap tm_cache;
     int raw_g;           // > 0: the fused path reads raw blocks through raw_maps
@@ -129,9 +130,18 @@ bool log_on()
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// F32 / F16 / BF16: the weight is already a matrix of floats; its f16 form
+// is the GEMM operand directly, so it has no fused path of its own.
+bool is_float_type(int type) { return type == MQ_TYPE_F32 || type == MQ_TYPE_F16 || type == MQ_TYPE_BF16; }
+
+const char *kTypeList = "F32=0, F16=1, Q4_0=2, Q5_0=6, Q5_1=7, Q8_0=8, Q4_K=12, Q5_K=13, Q6_K=14, BF16=30";
+
 bool block_format(int type, int &qk, int &bb)
 {
     switch (type) {
+    case MQ_TYPE_F32: qk = 1; bb = 4; return true;
+    case MQ_TYPE_F16: qk = 1; bb = 2; return true;
+    case MQ_TYPE_BF16: qk = 1; bb = 2; return true;
     case MQ_TYPE_Q4_0: qk = 32; bb = 18; return true;
     case MQ_TYPE_Q5_0: qk = 32; bb = 22; return true;
     case MQ_TYPE_Q5_1: qk = 32; bb = 24; return true;
@@ -503,10 +513,8 @@ int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, ui
     *out = nullptr;
     int qk = 0, bb = 0;
     if (!block_format(type, qk, bb))
-        return fail(MQ_ERR_UNSUPPORTED_TYPE,
-                    "type id %d is not supported (supported: Q4_0=2, Q5_0=6, Q5_1=7, Q8_0=8, Q4_K=12, Q5_K=13, "
-                    "Q6_K=14); the weight has no kernel",
-                    (int)type);
+        return fail(MQ_ERR_UNSUPPORTED_TYPE, "type id %d is not supported (supported: %s); the weight has no kernel",
+                    (int)type, kTypeList);
     if (flags & ~(MQ_REG_NO_CACHE | MQ_REG_NO_KPAD | MQ_REG_KPAD))
         return fail(MQ_ERR_INVALID, "unknown flag bits 0x%x", flags);
     if ((flags & MQ_REG_NO_KPAD) && (flags & MQ_REG_KPAD))
@@ -521,6 +529,9 @@ int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, ui
         return fail(MQ_ERR_SHAPE, "N*K=%lld is not a whole number of %d-element blocks", (long long)(N * K), qk);
     if (!aligned16(qdata))
         return fail(MQ_ERR_ALIGN, "qdata=%p is not 16-byte aligned", qdata);
+    if ((flags & MQ_REG_NO_CACHE) && (type == MQ_TYPE_F32 || type == MQ_TYPE_BF16))
+        return fail(MQ_ERR_INVALID, "type %d: an F32 or BF16 weight is read through its f16 copy; MQ_REG_NO_CACHE "
+                                    "applies to block formats and F16", (int)type);
 
     DevState *d = nullptr;
     int dev = 0;
@@ -551,11 +562,22 @@ int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, ui
     w->nblocks = N * K / qk;
     w->qdata = static_cast<const uint8_t *>(qdata);
     w->cache = nullptr;
+    w->cache_owned = false;
     w->device = dev;
     w->raw_g = env_int("MQ_RAW_TMA", 1) ? mq::encode_raw_maps(&w->raw_maps, qdata, type, N, K) : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (!(flags & MQ_REG_NO_CACHE)) {
+    if (type == MQ_TYPE_F16 && (ldk == K || (flags & MQ_REG_NO_CACHE))) {
+        // An F16 weight whose rows need no padding is the GEMM operand as it
+        // stands: read it in place (no copy, nothing allocated).
+        w->ldk = K;
+        w->cache = static_cast<__half *>(const_cast<void *>(qdata));
+        CUresult cr = mq::encode_f16_2d(&w->tm_cache, w->cache, N, K, K, 64, 128);
+        if (cr != CUDA_SUCCESS) {
+            delete w;
+            return fail(MQ_ERR_CUDA, "tensor map for the F16 weight: CUresult %d", (int)cr);
+        }
+    } else if (!(flags & MQ_REG_NO_CACHE)) {
         const size_t bytes = static_cast<size_t>(N) * static_cast<size_t>(ldk) * 2;
         void *p = nullptr;
         cudaError_t e = env_int("MQ_FAULT_ALLOC", 0) ? cudaErrorMemoryAllocation : cudaMalloc(&p, bytes);
@@ -566,6 +588,7 @@ int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, ui
                         (long long)ldk, cudaGetErrorString(e));
         }
         w->cache = static_cast<__half *>(p);
+        w->cache_owned = true;
         const int64_t tr = trace_begin(s, MQ_TRACE_DECODE, type, 0, N, K);
         e = mq::launch_dequant(type, qdata, w->nblocks, w->cache, K, ldk, s);
         trace_mark(tr, 1, s);
@@ -605,7 +628,7 @@ int mq_release_weight(mq_handle w)
             return fail(MQ_ERR_INVALID, "handle %p is not a live registered weight", (void *)w);
         g_live.erase(w);
     }
-    if (w->cache) {
+    if (w->cache && w->cache_owned) {
         int cur = 0;
         cudaGetDevice(&cur);
         cudaSetDevice(w->device);
@@ -633,9 +656,7 @@ int mq_dequantize(mq_type type, const void *qdata, int64_t N, int64_t K, void *o
 {
     int qk = 0, bb = 0;
     if (!block_format(type, qk, bb))
-        return fail(MQ_ERR_UNSUPPORTED_TYPE,
-                    "type id %d is not supported (Q4_0=2, Q5_0=6, Q5_1=7, Q8_0=8, Q4_K=12, Q5_K=13, Q6_K=14)",
-                    (int)type);
+        return fail(MQ_ERR_UNSUPPORTED_TYPE, "type id %d is not supported (%s)", (int)type, kTypeList);
     if (!qdata || !out_f16)
         return fail(MQ_ERR_INVALID, "%s is NULL", qdata ? "out_f16" : "qdata");
     if (N < 1 || K < 8 || (K % 8) != 0 || ldo < K || (ldo % 8) != 0)
@@ -709,6 +730,8 @@ int mq_gemm_fused(const void *x, mq_handle w, float *y, int64_t M, void *stream)
     int rc = check_gemm_args(x, w, y, M);
     if (rc)
         return rc;
+    if (is_float_type(w->type))   // nothing to decode on chip: the f16 operand exists
+        return run_gemm(x, w, y, M, static_cast<cudaStream_t>(stream), false);
     if (w->K % 64 != 0)
         return fail(MQ_ERR_SHAPE, "fused path needs K %% 64 == 0 (K=%lld)", (long long)w->K);
     if (w->raw_g == 0 && (w->nblocks * w->bb) % 16 != 0)
@@ -726,6 +749,40 @@ int mq_gemm_auto(const void *x, mq_handle w, float *y, int64_t M, void *stream)
     if (!w->cache || (M < current_gate() && fused_ok))
         return mq_gemm_fused(x, w, y, M, stream);
     return mq_gemm(x, w, y, M, stream);
+}
+
+int mq_gemm_scratch(const void *x, mq_handle w, float *y, int64_t M, void *scratch, int64_t scratch_bytes,
+                    void *stream)
+{
+    int rc = check_gemm_args(x, w, y, M);
+    if (rc)
+        return rc;
+    if (!scratch)
+        return fail(MQ_ERR_INVALID, "scratch is NULL");
+    if (!aligned16(scratch))
+        return fail(MQ_ERR_ALIGN, "scratch=%p is not 16-byte aligned", scratch);
+    const int64_t need = 2 * w->N * w->ldk;
+    if (scratch_bytes < need)
+        return fail(MQ_ERR_SHAPE, "scratch of %lld bytes; the f16 [N=%lld, ldk=%lld] weight needs %lld",
+                    (long long)scratch_bytes, (long long)w->N, (long long)w->ldk, (long long)need);
+    DevState *d = nullptr;
+    rc = device_state(&d);
+    if (rc)
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    mq_weight tmp = *w;
+    tmp.cache = static_cast<__half *>(scratch);
+    tmp.cache_owned = false;
+    CUresult cr = mq::encode_f16_2d(&tmp.tm_cache, tmp.cache, w->N, w->K, w->ldk, 64, 128);
+    if (cr != CUDA_SUCCESS)
+        return fail(MQ_ERR_CUDA, "tensor map for the scratch: CUresult %d", (int)cr);
+    const int64_t tr = trace_begin(s, MQ_TRACE_DECODE, w->type, M, w->N, w->K);
+    cudaError_t e = mq::launch_dequant(w->type, w->qdata, w->nblocks, tmp.cache, w->K, w->ldk, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode into the scratch");
+    trace_mark(tr, 1, s);
+    trace_mark(tr, 2, s);
+    return run_gemm(x, &tmp, y, M, s, false);
 }
 
 int64_t mq_get_m_gate(void) { return current_gate(); }

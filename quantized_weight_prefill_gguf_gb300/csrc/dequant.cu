@@ -1,10 +1,19 @@
-// dequant.cu -- standalone sm_103a block decoders Q4_K / Q6_K / Q8_0 -> f16.
+// dequant.cu -- standalone sm_103a decoders -> f16: the block formats Q4_0,
+// Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K, and the float weights F32 / F16 / BF16
+// (a conversion; the f16 copy then carries the row padding below).
 //
 // The f16 cache is filled by these kernels once, at registration ("05 · 8p —
 // Persistent f16 weight cache + fused dequant-in-GEMM", section 3.1: decode
 // at load, keep the f16 copy resident).  The work is a streaming pass: read
 // each block once, write 2 bytes per element once, so HBM bandwidth bounds
-// it (algorithmic bytes per element: 0.5625+2, 0.8203+2, 1.0625+2).
+// it (algorithmic bytes per element: block bytes / block length + 2, e.g.
+// Q4_K 0.5625+2, Q6_K 0.8203+2, Q8_0 1.0625+2; F32 4+2, F16 and BF16 2+2).
+//
+// Float weights ("ggml-cuda: GEMM weight row padding + one-time K-padded f16
+// dequant for prefill", Summary: pad a float weight's rows by one 128-byte
+// line when its row size is a multiple of 2048 bytes, so consecutive rows do
+// not collide in the same cache sets) are converted into the same K-padded
+// f16 layout the block formats decode into.
 //
 // Data movement.  Q6_K (210 B) and Q8_0 (34 B) blocks are only 2-byte
 // aligned, so a wide load at a block-relative offset can be misaligned (the
@@ -275,6 +284,93 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *__restrict_
     }
 }
 
+// Float weights: F32 (type 0), F16 (1), BF16 (30).  One f16 per element,
+// round to nearest even (F16 is copied bit for bit; a BF16 value widens
+// exactly to f32 first).  Piece v is elements 8v .. 8v+7 of the flat stream
+// (K % 8 == 0, so the eight share a row), stored as one 16-byte write;
+// consecutive threads take consecutive pieces on both sides.  Each thread
+// has kConvPieces pieces, kConvThreads apart, with all loads in flight
+// before the first store.
+constexpr int kConvThreads = 256;
+constexpr int kConvPieces = 4;
+
+template <int T>
+__device__ __forceinline__ uint4 convert_piece(const uint8_t *src)
+{
+    if constexpr (T == 1) {
+        return ldg_nc_v4(src);
+    } else if constexpr (T == 30) {
+        const uint4 b = ldg_nc_v4(src);
+        const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+        uint32_t r[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            r[i] = cvt_f16x2(f32x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u)));
+        return make_uint4(r[0], r[1], r[2], r[3]);
+    } else {
+        const uint4 a = ldg_nc_v4(src), b = ldg_nc_v4(src + 16);
+        return make_uint4(cvt_f16x2(f32x2(__uint_as_float(a.x), __uint_as_float(a.y))),
+                          cvt_f16x2(f32x2(__uint_as_float(a.z), __uint_as_float(a.w))),
+                          cvt_f16x2(f32x2(__uint_as_float(b.x), __uint_as_float(b.y))),
+                          cvt_f16x2(f32x2(__uint_as_float(b.z), __uint_as_float(b.w))));
+    }
+}
+
+template <int T>
+__global__ void __launch_bounds__(kConvThreads) k_convert(const uint8_t *__restrict__ q, uint32_t npieces,
+                                                         __half *__restrict__ out, int64_t ldo, int mode,
+                                                         BlockRows pr)
+{
+    constexpr int kSrcBytes = T == 0 ? 32 : 16;
+    const uint32_t v0 = blockIdx.x * (kConvThreads * kConvPieces) + threadIdx.x;
+    uint4 y[kConvPieces];
+#pragma unroll
+    for (int i = 0; i < kConvPieces; ++i) {
+        const uint32_t v = v0 + i * kConvThreads;
+        if (v < npieces)
+            y[i] = convert_piece<T>(q + static_cast<int64_t>(v) * kSrcBytes);
+    }
+    grid_dep_launch();
+    grid_dep_wait();   // the output may be read by the previous kernel on the stream
+#pragma unroll
+    for (int i = 0; i < kConvPieces; ++i) {
+        const uint32_t v = v0 + i * kConvThreads;
+        if (v < npieces) {
+            __half *dst;
+            if (mode == 0) {
+                dst = out + static_cast<int64_t>(v) * 8;
+            } else {
+                uint32_t n, c;
+                block_row(v, pr, n, c);
+                dst = out + static_cast<int64_t>(n) * ldo + static_cast<int64_t>(c) * 8;
+            }
+            stg_v4(dst, y[i]);
+        }
+    }
+}
+
+template <int T>
+cudaError_t launch_convert(const void *q, int64_t nelem, __half *out, int64_t K, int64_t ldo, cudaStream_t s)
+{
+    const int64_t npieces = nelem / 8;
+    if (npieces > 0xFFFFFFFFLL - kConvThreads * kConvPieces || K % 8 != 0)
+        return cudaErrorInvalidValue;
+    const int64_t per_cta = kConvThreads * kConvPieces;
+    BlockRows pr{1u, 0xFFFFFFFFu};
+    int mode = 0;
+    if (ldo != K) {
+        mode = 1;
+        pr.bpr = static_cast<uint32_t>(K / 8);
+        pr.m = 0xFFFFFFFFu / pr.bpr;
+    }
+    const cudaError_t e =
+        launch_kernel(k_convert<T>, dim3(static_cast<unsigned>((npieces + per_cta - 1) / per_cta)),
+                      dim3(kConvThreads), 0, s, static_cast<const uint8_t *>(q), static_cast<uint32_t>(npieces),
+                      out, ldo, mode, pr);
+    note_launch();
+    return e;
+}
+
 template <int T>
 cudaError_t launch_t(const void *q, int64_t nblocks, __half *out, int64_t K, int64_t ldo, cudaStream_t s)
 {
@@ -305,6 +401,9 @@ cudaError_t launch_dequant(int type, const void *q, int64_t nblocks, __half *out
     if (nblocks <= 0)
         return cudaSuccess;
     switch (type) {
+    case 0: return launch_convert<0>(q, nblocks, out, K, ldo, s);
+    case 1: return launch_convert<1>(q, nblocks, out, K, ldo, s);
+    case 30: return launch_convert<30>(q, nblocks, out, K, ldo, s);
     case 2: return launch_t<2>(q, nblocks, out, K, ldo, s);
     case 6: return launch_t<6>(q, nblocks, out, K, ldo, s);
     case 7: return launch_t<7>(q, nblocks, out, K, ldo, s);

@@ -23,6 +23,10 @@ drawn in the listed order, then the activations):
   0 and 2, qh at byte 4, 16 nibble bytes at byte 8.
 * Q5_K block (176 B): d, dmin as Q4_K at bytes 0 and 2, 12 scale/min bytes
   at 4, 32 qh bytes at 16, 128 nibble bytes at 48 (uniform bytes).
+* Float weights: values ~ N(0, 0.02) drawn in f32; F32 stores them, F16
+  stores them rounded to f16 (numpy's conversion), BF16 stores the upper
+  16 bits of each f32 draw (the distribution is defined that way: no
+  rounding step).
 * Activations X[M,K] ~ N(0,1) in f32, rounded to f16.
 
 Draw order inside a weight: Q4_K d, dmin, scale bytes, nibble bytes;
@@ -36,10 +40,11 @@ from dataclasses import dataclass
 
 import numpy as np
 
+F32, F16, BF16 = 0, 1, 30
 Q4_0, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 6, 7, 8, 12, 13, 14
-BLOCK = {Q4_0: (32, 18), Q5_0: (32, 22), Q5_1: (32, 24), Q8_0: (32, 34), Q4_K: (256, 144),
+BLOCK = {F32: (1, 4), F16: (1, 2), BF16: (1, 2), Q4_0: (32, 18), Q5_0: (32, 22), Q5_1: (32, 24), Q8_0: (32, 34), Q4_K: (256, 144),
          Q5_K: (256, 176), Q6_K: (256, 210)}
-TYPE_NAME = {Q4_0: "q4_0", Q5_0: "q5_0", Q5_1: "q5_1", Q8_0: "q8_0", Q4_K: "q4_K", Q5_K: "q5_K",
+TYPE_NAME = {F32: "f32", F16: "f16", BF16: "bf16", Q4_0: "q4_0", Q5_0: "q5_0", Q5_1: "q5_1", Q8_0: "q8_0", Q4_K: "q4_K", Q5_K: "q5_K",
              Q6_K: "q6_K"}
 
 
@@ -135,7 +140,20 @@ def q5_K_blocks(g: np.random.Generator, nblocks: int) -> np.ndarray:
     return b.reshape(-1)
 
 
-_DRAW = {Q4_K: q4_K_blocks, Q6_K: q6_K_blocks, Q8_0: q8_0_blocks, Q4_0: q4_0_blocks, Q5_0: q5_0_blocks,
+def f32_elems(g: np.random.Generator, n: int) -> np.ndarray:
+    return g.normal(0.0, 0.02, n).astype("<f4").view(np.uint8)
+
+
+def f16_elems(g: np.random.Generator, n: int) -> np.ndarray:
+    return g.normal(0.0, 0.02, n).astype(np.float32).astype("<f2").view(np.uint8)
+
+
+def bf16_elems(g: np.random.Generator, n: int) -> np.ndarray:
+    upper = (g.normal(0.0, 0.02, n).astype("<f4").view("<u4") >> 16).astype("<u2")
+    return upper.view(np.uint8)
+
+
+_DRAW = {F32: f32_elems, F16: f16_elems, BF16: bf16_elems, Q4_K: q4_K_blocks, Q6_K: q6_K_blocks, Q8_0: q8_0_blocks, Q4_0: q4_0_blocks, Q5_0: q5_0_blocks,
          Q5_1: q5_1_blocks, Q5_K: q5_K_blocks}
 
 
@@ -176,6 +194,10 @@ Q8_0_PAIR = [("w1", Q8_0, 3584, 18944), ("w2", Q8_0, 18944, 3584)]
 SINGLE_896 = [("w", Q4_K, 896, 896)]
 # The other block formats (Q4_0 / Q5_0 / Q5_1 / Q5_K), each at the 7B gate
 # (18944 x 3584) and down (3584 x 18944) shapes.
+# Float weights at the Llama-3.1-8B layer's shapes (K = 4096 and 14336 rows
+# are multiples of 2048 bytes in f16, so their copies are row-padded).
+FLOAT_LAYER = [(f"{TYPE_NAME[t]}_{nm}", t, n, k) for t in (F16, BF16)
+               for nm, n, k in (("q", 4096, 4096), ("gate", 14336, 4096), ("down", 4096, 14336))]
 MORE_FORMATS = [(f"{TYPE_NAME[t]}_{nm}", t, n, k) for t in (Q4_0, Q5_0, Q5_1, Q5_K)
                 for nm, n, k in (("gate", 18944, 3584), ("down", 3584, 18944))]
 
@@ -186,6 +208,7 @@ WORKLOADS = {
     "llama3.1-8b_layer": (LLAMA31_8B, [512]),
     "q8_0_pair": (Q8_0_PAIR, [128, 1024]),
     "more_formats": (MORE_FORMATS, [32, 2048]),
+    "float_layer": (FLOAT_LAYER, [512]),
     "small_m_sweep": ([w for w in QWEN25_7B if w[0] in ("gate", "up", "down")],
                       [1, 8, 32, 128, 256, 512, 2048]),
 }

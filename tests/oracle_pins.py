@@ -7,7 +7,8 @@ test runs them against deliberately broken copies of it to show that every
 planted mistake is caught by at least one pin.
 
 Block layouts pinned here are the GGUF convention for Q8_0 / Q4_K / Q6_K and
-Q4_0 / Q5_0 / Q5_1 / Q5_K; the pages name the types and block sizes (and
+Q4_0 / Q5_0 / Q5_1 / Q5_K, plus the float weights F32 / F16 / BF16 (stored
+little-endian, one element each); the pages name the types and block sizes (and
 Q5_0's fields) only ("05 · 8p — Persistent f16 weight cache + fused
 dequant-in-GEMM", sections 1 and 2).  Hand-built blocks below
 are written byte by byte from that layout, independently of the oracle's
@@ -20,6 +21,7 @@ from fractions import Fraction
 
 import numpy as np
 
+F32, F16, BF16 = 0, 1, 30
 Q4_0, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 6, 7, 8, 12, 13, 14
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -625,6 +627,74 @@ def pin_q5k_double_rounding(orc):
     out = orc.decode(Q5_K, q5k_bytes(f16bits(293 / 2048), 0x0001, S, [0] * 32, [7] + [0] * 127))
     assert int(out[0]) == 0x3C02, hex(int(out[0]))
     assert np.all(out[1:32] == 0x8001) and np.all(out[32:] == 0)
+
+
+def _decode_words(orc, qtype, words, width):
+    raw = b"".join(int(w).to_bytes(width, "little") for w in words)
+    return orc.decode(qtype, np.frombuffer(raw, dtype=np.uint8))
+
+
+def pin_f16_passthrough(orc):
+    """An F16 weight's f16 value is the element itself: all 65536 patterns,
+    stored little-endian, come back unchanged (NaN payloads included)."""
+    allbits = np.arange(65536, dtype=np.uint32)
+    assert np.array_equal(_decode_words(orc, F16, allbits, 2), allbits.astype(np.uint16))
+
+
+# (bfloat16 bits, binary16 bits, reason)
+BF16_CASES = [
+    (0x3F80, 0x3C00, "1.0"),
+    (0xBF80, 0xBC00, "-1.0"),
+    (0x3F81, 0x3C08, "1 + 2^-7: exact, mantissa 8 * 2^-10"),
+    (0x477F, 0x7BF8, "65280 = 255 * 2^8: exact, exponent 15, mantissa 1016 / 1024"),
+    (0x4780, 0x7C00, "65536: past the binary16 maximum 65504 and the half-way point 65520: infinity"),
+    (0xFF80, 0xFC00, "-infinity"),
+    (0x8000, 0x8000, "-0 keeps its sign"),
+    (0x3880, 0x0400, "2^-14: the smallest binary16 normal"),
+    (0x3380, 0x0001, "2^-24: the smallest binary16 subnormal"),
+    (0x3300, 0x0000, "2^-25: half the smallest subnormal, a tie, to even 0"),
+    (0x3340, 0x0001, "0.75 * 2^-24: above the half-way point, up"),
+    (0x3420, 0x0002, "2.5 * 2^-24: a tie, to even 2"),
+    (0x3460, 0x0004, "3.5 * 2^-24: a tie, to even 4"),
+    (0x35FF, 0x0020, "31.875 * 2^-24 (2^-20 * 255/128): rounds to 32 * 2^-24"),
+]
+
+# (binary32 bits, binary16 bits, reason)
+F32_CASES = [
+    (0x3F800000, 0x3C00, "1.0"),
+    (0xC0490FDB, 0xC248, "-pi: mantissa (pi/2 - 1) * 1024 = 584.495 rounds to 584, -3.140625"),
+    (0x477FEFFF, 0x7BFF, "65519.996: just below the half-way point to infinity, 65504"),
+    (0x477FF000, 0x7C00, "65520: a tie between 65504 (odd significand) and 2^16, to even: infinity"),
+    (0x80000000, 0x8000, "-0"),
+    (0x3F801000, 0x3C00, "1 + 2^-11: a tie, to even 1.0"),
+    (0x3F803000, 0x3C02, "1 + 3 * 2^-11: a tie, to even 1 + 2^-9"),
+    (0x33000000, 0x0000, "2^-25: a tie, to even 0"),
+    (0x33000001, 0x0001, "2^-25 (1 + 2^-23): above the tie, the smallest subnormal"),
+    (0x7F800000, 0x7C00, "infinity"),
+]
+
+
+def pin_bf16_values(orc):
+    """BF16 elements: the upper half of a binary32, rounded to binary16 as
+    the table's reasons say (decoded as one little-endian stream)."""
+    got = _decode_words(orc, BF16, [c[0] for c in BF16_CASES], 2)
+    for (src, want, why), g in zip(BF16_CASES, got):
+        assert int(g) == want, f"bf16 0x{src:04x} ({why}): got 0x{int(g):04x} want 0x{want:04x}"
+
+
+def pin_f32_values(orc):
+    """F32 elements rounded to binary16 as the table's reasons say (decoded
+    as one little-endian stream, four bytes per element)."""
+    got = _decode_words(orc, F32, [c[0] for c in F32_CASES], 4)
+    for (src, want, why), g in zip(F32_CASES, got):
+        assert int(g) == want, f"f32 0x{src:08x} ({why}): got 0x{int(g):04x} want 0x{want:04x}"
+
+
+def pin_float_nan_stays_nan(orc):
+    """A NaN element (F32 or BF16) decodes to a binary16 NaN."""
+    for qt, words, width in ((F32, [0x7FC00000, 0xFF800001, 0x7F800400], 4), (BF16, [0x7FC0, 0xFF81], 2)):
+        out = _decode_words(orc, qt, words, width)
+        assert np.all((out & 0x7C00) == 0x7C00) and np.all((out & 0x03FF) != 0), (qt, out)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

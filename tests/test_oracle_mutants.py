@@ -51,6 +51,12 @@ MUTANTS = {
     "q5k_qh_offset": ("const uint8_t *qh = b + 16;\n    const uint8_t *qs = b + 48;", "const uint8_t *qh = b + 48;\n    const uint8_t *qs = b + 16;"),
     "q5k_wrong_subblock": ("q4k_scale_min(S, sub, &scale, &mn);", "q4k_scale_min(S, grp, &scale, &mn);"),
     "q5k_min_dropped": ("y[e] = oracle_f32_to_f16(prod - off);", "y[e] = oracle_f32_to_f16(prod);"),
+    "f32_big_endian": ("uint32_t x = (uint32_t)b[0] | ((uint32_t)b[1] << 8) | ((uint32_t)b[2] << 16) | ((uint32_t)b[3] << 24);",
+                       "uint32_t x = (uint32_t)b[3] | ((uint32_t)b[2] << 8) | ((uint32_t)b[1] << 16) | ((uint32_t)b[0] << 24);"),
+    "bf16_low_half": ("uint32_t x = (uint32_t)rd_u16le(b) << 16;", "uint32_t x = (uint32_t)rd_u16le(b);"),
+    "bf16_read_as_f16": ("case T_BF16: y[0] = decode_bf16_elem(b); break;", "case T_BF16: y[0] = rd_u16le(b); break;"),
+    "f16_bytes_swapped": ("case T_F16:  y[0] = rd_u16le(b); break;",
+                          "case T_F16:  y[0] = (uint16_t)((b[0] << 8) | b[1]); break;"),
     "gemm_reversed_operand": ("acc += x[k] * w[k];", "acc += x[k] * w[K - 1 - k];"),
     "gemm_f32_accumulator": ("double acc = 0.0;", "float acc = 0.0f;"),
     "gemm_drops_last_term": ("for (int64_t k = 0; k < K; k++)\n        acc += x[k] * w[k];",
