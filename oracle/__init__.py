@@ -69,6 +69,16 @@ class Oracle:
         L.oracle_gemm_f64_sampled.argtypes = [_P, _I64, _P, _P, _P, _I64, _P]
         L.oracle_gemm_f64_sampled.restype = ctypes.c_int
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+        L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_to_f64.restype = ctypes.c_double
+        L.oracle_quantize_e4m3_rows.argtypes = [_P, _I64, _I64, _I64, _P, _P]
+        L.oracle_quantize_e4m3_rows.restype = ctypes.c_int
+        L.oracle_gemm_e4m3_f64.argtypes = [_P, _P, _I64, _I64, _P, _P, _I64, _P]
+        L.oracle_gemm_e4m3_f64.restype = ctypes.c_int
+        L.oracle_gemm_e4m3_f64_sampled.argtypes = [_P, _P, _I64, _P, _P, _P, _P, _I64, _P]
+        L.oracle_gemm_e4m3_f64_sampled.restype = ctypes.c_int
         L.oracle_pack_q8_0.argtypes = [ctypes.c_uint16, _P, _P]
         L.oracle_pack_q4_K.argtypes = [ctypes.c_uint16, ctypes.c_uint16, _P, _P, _P, _P]
         L.oracle_pack_q6_K.argtypes = [ctypes.c_uint16, _P, _P, _P]
@@ -134,6 +144,56 @@ class Oracle:
                                             out.ctypes.data)
         if rc:
             raise MemoryError("oracle_gemm_f64_sampled failed")
+        return out
+
+    # -- O5 -----------------------------------------------------------
+    def f32_to_e4m3(self, x) -> np.ndarray:
+        """e4m3 codes of binary32 values (round to nearest even, clamp to 448)."""
+        x = np.asarray(x, dtype=np.float32).reshape(-1)
+        return np.array([self.L.oracle_f32_to_e4m3(float(v)) for v in x], dtype=np.uint8)
+
+    def e4m3_to_f64(self, codes) -> np.ndarray:
+        codes = np.asarray(codes, dtype=np.uint8).reshape(-1)
+        return np.array([self.L.oracle_e4m3_to_f64(int(c)) for c in codes], dtype=np.float64)
+
+    def quantize_e4m3_rows(self, X16):
+        """Row-wise e4m3 quantization of f16 bits [rows, K]: (codes [rows, K]
+        uint8, scales [rows] float32)."""
+        X16 = np.ascontiguousarray(X16, dtype=np.uint16)
+        rows, K = X16.shape
+        q = np.empty((rows, K), dtype=np.uint8)
+        sc = np.empty(rows, dtype=np.float32)
+        self.L.oracle_quantize_e4m3_rows(X16.ctypes.data, rows, K, K, q.ctypes.data, sc.ctypes.data)
+        return q, sc
+
+    def gemm_e4m3_f64(self, X8, sx, W8, sw) -> np.ndarray:
+        """Y = (x8 . w8^T) * sw[n] * sx[m] in f64."""
+        X8 = np.ascontiguousarray(X8, dtype=np.uint8)
+        W8 = np.ascontiguousarray(W8, dtype=np.uint8)
+        sx = np.ascontiguousarray(sx, dtype=np.float32)
+        sw = np.ascontiguousarray(sw, dtype=np.float32)
+        M, K = X8.shape
+        N, K2 = W8.shape
+        assert K == K2 and sx.size == M and sw.size == N
+        Y = np.empty((M, N), dtype=np.float64)
+        self.L.oracle_gemm_e4m3_f64(X8.ctypes.data, sx.ctypes.data, M, K, W8.ctypes.data, sw.ctypes.data, N,
+                                    Y.ctypes.data)
+        return Y
+
+    def gemm_e4m3_f64_sampled(self, X8, sx, W8, sw, mi, ni) -> np.ndarray:
+        X8 = np.ascontiguousarray(X8, dtype=np.uint8)
+        W8 = np.ascontiguousarray(W8, dtype=np.uint8)
+        sx = np.ascontiguousarray(sx, dtype=np.float32)
+        sw = np.ascontiguousarray(sw, dtype=np.float32)
+        mi = np.ascontiguousarray(mi, dtype=np.int64)
+        ni = np.ascontiguousarray(ni, dtype=np.int64)
+        K = X8.shape[1]
+        assert W8.shape[1] == K and mi.shape == ni.shape
+        assert mi.size == 0 or (mi.min() >= 0 and mi.max() < X8.shape[0])
+        assert ni.size == 0 or (ni.min() >= 0 and ni.max() < W8.shape[0])
+        out = np.empty(mi.size, dtype=np.float64)
+        self.L.oracle_gemm_e4m3_f64_sampled(X8.ctypes.data, sx.ctypes.data, K, W8.ctypes.data, sw.ctypes.data,
+                                            mi.ctypes.data, ni.ctypes.data, mi.size, out.ctypes.data)
         return out
 
     def num_threads(self) -> int:

@@ -36,6 +36,19 @@
  *      own value; a BF16 element is the upper half of a binary32 whose lower
  *      half is zero, widened exactly and then rounded as an F32 element is.
  *
+ *  O5  The 8-bit variant (the MMQ idea of "Eager GPU Offload Without A
+ *      Compute Graph", section "F16 and GGUF quantized linears": quantize
+ *      the activations once per call, run the MMA on 8-bit operands, scale
+ *      afterwards; with e4m3 floats in place of int8).  e4m3 is the OCP
+ *      8-bit float: sign, 4 exponent bits (bias 7), 3 mantissa bits, no
+ *      infinities, the all-ones code the only NaN (largest finite 448),
+ *      subnormals m * 2^-9.  A row of f16 values gets one binary32 scale
+ *      s = RN32(amax / 448) and codes e4m3(RN32(v * RN32(448 / amax)))
+ *      (s = 1 for an all-zero row); rounding to e4m3 is to nearest even on
+ *      the exact value, finite values past 448 clamp to 448.  The variant's
+ *      product is Y[m,n] = (sum_k x8[m,k] * w8[n,k]) * sw[n] * sx[m], here
+ *      in f64.  Inputs are assumed finite.
+ *
  *  O4  GEMM with f64 accumulation in k order: Y[m,n] = sum_k X[m,k]*W[n,k]
  *      for f16 X and the f16 dequantized W, the product the pages check
  *      their kernels against ("Eager GPU Offload Without A Compute Graph",
@@ -430,6 +443,112 @@ int oracle_gemm_f64_sampled(const uint16_t *X, int64_t K, const uint16_t *W,
         free(wd);
     }
     return err ? -2 : 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* O5: e4m3 codes, row quantization, the 8-bit GEMM                   */
+/* ------------------------------------------------------------------ */
+
+/* Nearest integer to u >= 0, ties to even (u is exact in double). */
+static double round_half_even(double u)
+{
+    double r = floor(u);
+    double frac = u - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0))
+        r += 1.0;
+    return r;
+}
+
+uint8_t oracle_f32_to_e4m3(float f)
+{
+    if (isnan(f))
+        return 0x7F;
+    const uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    const double a = fabs((double)f);
+    if (a == 0.0)
+        return sign;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: units of 2^-9; a count of 8 is the smallest
+         * normal 2^-6, whose code is 0x08 as well */
+        return (uint8_t)(sign | (uint8_t)round_half_even(a * 512.0));
+    }
+    int e;
+    double m = frexp(a, &e); /* a = m * 2^e, m in [0.5, 1) */
+    m *= 2.0;
+    e -= 1;                  /* a = m * 2^e, m in [1, 2) */
+    double q = round_half_even(m * 8.0); /* significand in eighths: 8 .. 16 */
+    if (q == 16.0) {
+        q = 8.0;
+        e += 1;
+    }
+    if (e > 8 || (e == 8 && q > 14.0))
+        return (uint8_t)(sign | 0x7E); /* clamp to 448 */
+    return (uint8_t)(sign | (uint8_t)(((e + 7) << 3) | ((int)q - 8)));
+}
+
+double oracle_e4m3_to_f64(uint8_t b)
+{
+    const int e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    const double v = e ? ldexp((double)(8 + m), e - 10) : ldexp((double)m, -9);
+    return (b & 0x80) ? -v : v;
+}
+
+int oracle_quantize_e4m3_rows(const uint16_t *src, int64_t rows, int64_t K, int64_t ld, uint8_t *dst,
+                              float *scales)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++) {
+        const uint16_t *row = src + r * ld;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; k++) {
+            float v = fabsf(oracle_f16_to_f32(row[k]));
+            if (v > amax)
+                amax = v;
+        }
+        float s = 1.0f, inv = 1.0f;
+        if (amax > 0.0f) {
+            s = amax / 448.0f;
+            inv = 448.0f / amax;
+        }
+        for (int64_t k = 0; k < K; k++) {
+            float t = oracle_f16_to_f32(row[k]) * inv;
+            dst[r * K + k] = oracle_f32_to_e4m3(t);
+        }
+        scales[r] = s;
+    }
+    return 0;
+}
+
+/* Y[m,n] = (sum_k x8[m,k] * w8[n,k]) * sw[n] * sx[m]: each product of two
+ * e4m3 values is exact in double, the sum is taken in k order. */
+static double e4m3_dot_f64(const uint8_t *x, const uint8_t *w, int64_t K)
+{
+    double sum = 0.0;
+    for (int64_t k = 0; k < K; k++)
+        sum += oracle_e4m3_to_f64(x[k]) * oracle_e4m3_to_f64(w[k]);
+    return sum;
+}
+
+int oracle_gemm_e4m3_f64(const uint8_t *X8, const float *sx, int64_t M, int64_t K, const uint8_t *W8,
+                         const float *sw, int64_t N, double *Y)
+{
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = 0; n < N; n++)
+            Y[m * N + n] = e4m3_dot_f64(X8 + m * K, W8 + n * K, K) * (double)sw[n] * (double)sx[m];
+    return 0;
+}
+
+int oracle_gemm_e4m3_f64_sampled(const uint8_t *X8, const float *sx, int64_t K, const uint8_t *W8,
+                                 const float *sw, const int64_t *mi, const int64_t *ni, int64_t count,
+                                 double *out)
+{
+    #pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < count; i++)
+        out[i] = e4m3_dot_f64(X8 + mi[i] * K, W8 + ni[i] * K, K) * (double)sw[ni[i]] * (double)sx[mi[i]];
+    return 0;
 }
 
 /* Number of OpenMP threads a parallel region of this library uses. */

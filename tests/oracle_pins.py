@@ -697,4 +697,126 @@ def pin_float_nan_stays_nan(orc):
         assert np.all((out & 0x7C00) == 0x7C00) and np.all((out & 0x03FF) != 0), (qt, out)
 
 
+# (binary32 value, e4m3 code, reason) -- OCP e4m3: bias 7, 3 mantissa bits,
+# largest finite 448, subnormals m * 2^-9, round to nearest even, clamp.
+E4M3_CASES = [
+    (1.0, 0x38, "1.0: exponent field 7"),
+    (448.0, 0x7E, "448 = 1.75 * 2^8, the largest finite"),
+    (0.5, 0x30, "0.5: exponent field 6"),
+    (2.0 ** -9, 0x01, "the smallest subnormal"),
+    (2.0 ** -10, 0x00, "half the smallest subnormal: a tie, to even 0"),
+    (3 * 2.0 ** -10, 0x02, "1.5 * 2^-9: a tie between 1 and 2 units, to even 2"),
+    (2.0 ** -6, 0x08, "the smallest normal"),
+    (0.97 * 2.0 ** -6, 0x08, "7.76 units of 2^-9 round up to the smallest normal"),
+    (1.0625, 0x38, "halfway between 1 and 1.125: to even 1"),
+    (1.1875, 0x3A, "halfway between 1.125 and 1.25: to even 1.25"),
+    (240.0, 0x77, "240 = 1.875 * 2^7"),
+    (232.0, 0x76, "232 halfway between 224 and 240: to even 224"),
+    (464.0, 0x7E, "halfway between 448 and 480 (480 is not finite): to even 448"),
+    (480.0, 0x7E, "past 448 after rounding: clamped to 448"),
+    (1e9, 0x7E, "far past the range: clamped"),
+    (-1e9, 0xFE, "negative: clamped to -448"),
+    (-0.0, 0x80, "-0 keeps its sign"),
+    (-2.0 ** -11, 0x80, "a negative value that rounds to zero keeps its sign"),
+    (-224.0, 0xF6, "-224 = -1.75 * 2^7"),
+]
+
+
+def pin_e4m3_values(orc):
+    got = orc.f32_to_e4m3([c[0] for c in E4M3_CASES])
+    for (v, want, why), g in zip(E4M3_CASES, got):
+        assert int(g) == want, f"e4m3({v!r}) ({why}): got 0x{int(g):02x} want 0x{want:02x}"
+    assert int(orc.f32_to_e4m3([float("nan")])[0]) == 0x7F
+
+
+def pin_e4m3_decode(orc):
+    """Every code decodes to (8+m)*2^(e-10) (e > 0) or m*2^-9 (e = 0) with
+    its sign, 0x7F / 0xFF are NaN, and encoding a decoded value returns the
+    code (-0 included)."""
+    codes = np.arange(256, dtype=np.uint8)
+    vals = orc.e4m3_to_f64(codes)
+    for c, v in zip(codes.tolist(), vals.tolist()):
+        e, m = (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            assert np.isnan(v)
+            continue
+        mag = (8 + m) * 2.0 ** (e - 10) if e else m * 2.0 ** -9
+        assert v == (-mag if c & 0x80 else mag) and np.signbit(v) == bool(c & 0x80), c
+    finite = codes[~np.isnan(vals)]
+    assert np.array_equal(orc.f32_to_e4m3(orc.e4m3_to_f64(finite).astype(np.float32)), finite)
+
+
+def pin_e4m3_matches_torch(orc):
+    """Within +-464 (where no clamping happens) the encoder agrees with
+    PyTorch's CPU float8_e4m3fn conversion on every code's value, every
+    midpoint between neighbouring codes, the binary32 neighbours of each
+    midpoint, and 20000 log-uniform random values."""
+    torch = __import__("pytest").importorskip("torch")
+    vals = np.sort(orc.e4m3_to_f64(np.arange(0, 0x7F, dtype=np.uint8)))
+    mids = (vals[:-1] + vals[1:]) / 2
+    mids = np.append(mids, 464.0)
+    m32 = mids.astype(np.float32)
+    pts = np.concatenate([vals.astype(np.float32), m32, np.nextafter(m32, np.float32(0)),
+                          np.nextafter(m32, np.float32(1e9))])
+    g = np.random.Generator(np.random.PCG64(31))
+    rnd = (np.exp(g.uniform(np.log(2.0 ** -12), np.log(464.0), 20000))).astype(np.float32)
+    pts = np.concatenate([pts, rnd])
+    pts = pts[np.abs(pts) <= 464.0]
+    pts = np.concatenate([pts, -pts])
+    ref = torch.from_numpy(pts).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = orc.f32_to_e4m3(pts)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, first {pts[bad[0]]!r}: 0x{got[bad[0]]:02x} vs 0x{ref[bad[0]]:02x}"
+
+
+def pin_quantize_rows(orc):
+    """Hand rows: [2, -1, 0.5, 0] has amax 2, scale RN32(2/448), inv = 224 and
+    codes e4m3(448) = 0x7E, e4m3(-224) = 0xF6, e4m3(112) = 0x6E, 0; an all-zero
+    row has scale 1 and zero codes; a row whose amax is 448 keeps its values
+    (inv = 1); the amax is of magnitudes (a large negative value sets it)."""
+    rows = np.array([[2.0, -1.0, 0.5, 0.0], [0.0, 0.0, 0.0, 0.0], [448.0, 1.0, -3.0, 0.25],
+                     [-8.0, 1.0, 2.0, 4.0]], dtype=np.float16)
+    q, sc = orc.quantize_e4m3_rows(rows.view(np.uint16))
+    assert q[0].tolist() == [0x7E, 0xF6, 0x6E, 0x00]
+    assert sc[0] == np.float32(1 / 224)   # the binary32 nearest 1/224 (not near a tie)
+    assert q[1].tolist() == [0, 0, 0, 0] and sc[1] == 1.0
+    # inv = 1: 448 -> 0x7E, 1 -> 0x38, -3 = -1.5*2^1 -> 0xC4, 0.25 = 2^-2 -> 0x28
+    assert q[2].tolist() == [0x7E, 0x38, 0xC4, 0x28] and sc[2] == 1.0
+    # amax 8, inv = 56: -448 -> 0xFE, 56 = 1.75*2^5 -> 0x66, 112 -> 0x6E, 224 -> 0x76
+    assert q[3].tolist() == [0xFE, 0x66, 0x6E, 0x76] and sc[3] == np.float32(8 / 448)
+    # The multiplier is RN32(448 / amax), not 1 / s: amax = 1.765625 gives
+    # 448/amax = 253.7345132..., binary32 253.73451232910156; times v =
+    # 1.32421875 that is 336 - 1.3e-6, which rounds (binary32 spacing 3.05e-5
+    # there) to exactly 336, the e4m3 tie between 320 and 352: to even 320,
+    # 0x7A.  1/s = 253.73452758789062 would give 336.00003 and 0x7B.
+    q, sc = orc.quantize_e4m3_rows(np.array([[1.765625, 1.32421875]], dtype=np.float16).view(np.uint16))
+    assert q[0].tolist() == [0x7E, 0x7A]
+
+
+def pin_gemm_e4m3_exact(orc):
+    """Tiny random codes and scales: the oracle's f64 result equals the
+    exact rational value (Fractions) up to the two final f64 scalings."""
+    g = np.random.Generator(np.random.PCG64(32))
+    M, N, K = 3, 4, 40
+    X8 = g.integers(0, 256, (M, K)).astype(np.uint8)
+    W8 = g.integers(0, 256, (N, K)).astype(np.uint8)
+    X8[(X8 & 0x7F) == 0x7F] = 0x10   # no NaN codes
+    W8[(W8 & 0x7F) == 0x7F] = 0x11
+    sx = g.uniform(0.01, 2.0, M).astype(np.float32)
+    sw = g.uniform(0.01, 2.0, N).astype(np.float32)
+
+    def frac(c):
+        e, m = (c >> 3) & 15, c & 7
+        v = Fraction(8 + m) * Fraction(2) ** (e - 10) if e else Fraction(m) * Fraction(2) ** -9
+        return -v if c & 0x80 else v
+    Y = orc.gemm_e4m3_f64(X8, sx, W8, sw)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(frac(int(X8[m, k])) * frac(int(W8[n, k])) for k in range(K))
+            exact *= Fraction(float(sw[n])) * Fraction(float(sx[m]))
+            assert abs(Y[m, n] - float(exact)) <= 4e-16 * max(abs(float(exact)), 1e-300), (m, n)
+    mi = np.array([0, 2, 1]); ni = np.array([3, 0, 2])
+    assert np.array_equal(orc.gemm_e4m3_f64_sampled(X8, sx, W8, sw, mi, ni), Y[mi, ni])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

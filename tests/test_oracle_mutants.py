@@ -57,6 +57,14 @@ MUTANTS = {
     "bf16_read_as_f16": ("case T_BF16: y[0] = decode_bf16_elem(b); break;", "case T_BF16: y[0] = rd_u16le(b); break;"),
     "f16_bytes_swapped": ("case T_F16:  y[0] = rd_u16le(b); break;",
                           "case T_F16:  y[0] = (uint16_t)((b[0] << 8) | b[1]); break;"),
+    "e4m3_ties_away": ("if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0))", "if (frac >= 0.5)"),
+    "e4m3_no_clamp": ("if (e > 8 || (e == 8 && q > 14.0))", "if (e > 9)"),
+    "e4m3_bias_8": ("return (uint8_t)(sign | (uint8_t)(((e + 7) << 3) | ((int)q - 8)));",
+                    "return (uint8_t)(sign | (uint8_t)(((e + 8) << 3) | ((int)q - 8)));"),
+    "e4m3_subnormal_unit": ("round_half_even(a * 512.0)", "round_half_even(a * 1024.0)"),
+    "e4m3_quant_signed_amax": ("float v = fabsf(oracle_f16_to_f32(row[k]));", "float v = oracle_f16_to_f32(row[k]);"),
+    "e4m3_quant_inv_from_scale": ("inv = 448.0f / amax;", "inv = 1.0f / s;"),
+    "e4m3_gemm_drops_x_scale": ("* (double)sw[n] * (double)sx[m];", "* (double)sw[n];"),
     "gemm_reversed_operand": ("acc += x[k] * w[k];", "acc += x[k] * w[K - 1 - k];"),
     "gemm_f32_accumulator": ("double acc = 0.0;", "float acc = 0.0f;"),
     "gemm_drops_last_term": ("for (int64_t k = 0; k < K; k++)\n        acc += x[k] * w[k];",
