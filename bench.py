@@ -28,7 +28,11 @@ Printed: one JSON line (rank 0) with the contract keys plus
                 path, the per-call scratch mode and the fused path at M = 32
                 and 2048: time per layer and device bytes each mode holds;
   row_pad       F16 / BF16 weights of the Llama-3.1-8B layer's shapes at
-                M = 512, cached GEMM on the row-padded copy vs unpadded rows.
+                M = 512, cached GEMM on the row-padded copy vs unpadded rows;
+  e4m3          the same layer step through the 8-bit variant (its own
+                numeric contract): the four distinct activations quantized
+                per step, seven e4m3 GEMMs; TFLOP/s, the e4m3 kernel against
+                the 8-bit dense peak, distance to the f16 result.
 
 --impl reference times the CPU oracle itself as the reference arm.
 """
@@ -391,6 +395,7 @@ def main():
         out["more_formats"] = more_formats(mq, torch, stream, P)
         out["triangle"] = triangle(mq, torch, stream, weights, handles, qdev, xdev)
         out["row_pad"] = row_pad(mq, torch, stream)
+        out["e4m3"] = e4m3_layer(mq, torch, stream, weights, qdev, xdev, ys, P, min(args.steps, 400), flops_step)
     if rank == 0 and world == 1 and not args.no_extras:
         tf, tokens, secs, dsec, threads = oracle_cpu_run(weights, xs, args.cpu_seconds)
         out["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -627,6 +632,65 @@ def row_pad(mq, torch, stream):
     mq.mq_stream_status()
     return {"rows": res, "method": "back to back over R registered copies, each from its own weight buffer "
                                    "(an unpadded F16 weight is read in place)"}
+
+
+def e4m3_layer(mq, torch, stream, weights, qdev, xdev, ys_f16, P, steps, flops_step):
+    """The layer step on the 8-bit variant: per step the activations of the
+    four launch groups (q|k|v, o, gate|up, down) are quantized once each and
+    the seven GEMMs run on e4m3 operands.  Timed like the main loop (CUDA
+    events around `steps` steps after 5 warm-ups); the e4m3 kernel's mean
+    launch time comes from a traced pass."""
+    M = M_TOKENS
+    hs = [mq.mq_register_weight(w.qtype, q, w.N, w.K, flags=mq.MQ_REG_E4M3) for w, q in zip(weights, qdev)]
+    groups = [g for g in LAUNCH_GROUPS]
+    idx = {w.name: i for i, w in enumerate(weights)}
+    x8 = {}
+    for g in groups:
+        K = weights[idx[g[0]]].K
+        x8[g] = (torch.empty((M, K), dtype=torch.uint8, device="cuda"), torch.empty(M, dtype=torch.float32,
+                                                                                     device="cuda"))
+    ys = [torch.empty((M, w.N), dtype=torch.float32, device="cuda") for w in weights]
+
+    def step():
+        for g in groups:
+            K = weights[idx[g[0]]].K
+            q8, sx = x8[g]
+            mq.mq_quantize_e4m3(xdev[K][:M], q8, sx, stream)
+            for name in g:
+                i = idx[name]
+                mq.mq_gemm_e4m3(q8, sx, hs[i], ys[i], M, stream)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    mq.mq_trace_enable(True)
+    for _ in range(20):
+        step()
+    torch.cuda.synchronize()
+    recs = [r for r in mq.mq_trace_records() if r["kind"] == mq.MQ_TRACE_GEMM_CACHED]
+    mq.mq_trace_enable(False)
+    kern_flops = [2.0 * r["M"] * r["N"] * r["K"] for r in recs]
+    kern_ms = [r["ms_main"] for r in recs]
+    achieved = sum(kern_flops) / (sum(kern_ms) * 1e-3) / 1e12 if recs else None
+    peak8 = 2.0 * P["bf16_tflops"]
+    gi = idx["gate"]
+    dist = float(torch.linalg.norm(ys[gi] - ys_f16[gi]) / torch.linalg.norm(ys_f16[gi]))
+    mq.mq_stream_status()
+    for h in hs:
+        h.release()
+    return {"ms_per_step": ms, "tflops": flops_step / (ms * 1e-3) / 1e12, "steps": steps,
+            "kernel": {"name": "k_gemm_e4m3", "achieved_tflops": achieved, "peak_tflops": peak8,
+                       "peak_note": "8-bit dense = 2 x the measured bf16 burst peak (the nominal fp8:bf16 ratio)",
+                       "frac": achieved / peak8 if achieved else None},
+            "rel_distance_to_f16_gate": dist,
+            "note": "separate numeric contract: e4m3 operands with per-row / per-token f32 scales"}
 
 
 def decode_steady(mq, torch, stream, P):

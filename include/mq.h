@@ -85,6 +85,7 @@ typedef enum {
 #define MQ_REG_NO_CACHE 0x1u  /* build no f16 cache: only fused calls on this handle     */
 #define MQ_REG_NO_KPAD  0x2u  /* cache row stride ldk = K even when 2K % 2048 == 0       */
 #define MQ_REG_KPAD     0x4u  /* force ldk = K + 64                                      */
+#define MQ_REG_E4M3     0x8u  /* also build the e4m3 copy read by mq_gemm_e4m3           */
 
 typedef struct mq_weight *mq_handle;
 
@@ -235,6 +236,57 @@ int mq_gemm_auto(const void *x, mq_handle w, float *y, int64_t M, void *stream);
  */
 int mq_gemm_scratch(const void *x, mq_handle w, float *y, int64_t M, void *scratch,
                     int64_t scratch_bytes, void *stream);
+
+/*
+ * The 8-bit variant.  Passage: "Eager GPU Offload Without A Compute Graph",
+ * section "F16 and GGUF quantized linears" (the activation-quantized MMQ
+ * path: quantize each activation tile once to an 8-bit layout with scales,
+ * run the MMA on 8-bit operands; a separate numeric contract).  On this GPU
+ * the 8-bit operands are e4m3 floats (OCP: bias 7, 3 mantissa bits, largest
+ * finite 448) with one binary32 scale per row:
+ *
+ *     amax = max |v| over the row,  s = RN32(amax / 448),
+ *     code = e4m3_rn_satfinite(RN32(v * RN32(448 / amax)))
+ *
+ * (s = 1 and all codes 0 for an all-zero row), and
+ *
+ *     Y[m, n] = RN32(RN32(acc[m, n] * sw[n]) * sx[m]),
+ *     acc = sum_k x8[m, k] * w8[n, k] with f32 accumulation.
+ *
+ * The result differs from mq_gemm's by the quantization error (a few
+ * percent, relative); it is a separate contract, checked against the exact
+ * product of the quantized operands.  Inputs must be finite.
+ *
+ * mq_quantize_e4m3 -- quantize rows of an f16 matrix.
+ *  x       f16 [rows, K], row stride ld (ld >= K, ld % 8 == 0), device,
+ *          16-byte aligned.
+ *  dst     e4m3 codes [rows, K], row stride ldo bytes (ldo >= K, ldo % 16
+ *          == 0), device, 16-byte aligned; columns past K are not written.
+ *  scales  f32 [rows], device, 4-byte aligned.
+ *  K % 16 == 0.  Errors: MQ_ERR_INVALID, MQ_ERR_SHAPE, MQ_ERR_ALIGN,
+ *  MQ_ERR_CUDA.
+ */
+int mq_quantize_e4m3(const void *x, int64_t rows, int64_t K, int64_t ld, void *dst, int64_t ldo,
+                     float *scales, void *stream);
+
+/*
+ * mq_gemm_e4m3 -- Y = (x8 . w8^T) * sw[n] * sx[m] (see above) on the weight's
+ * e4m3 copy (registered with MQ_REG_E4M3: the f16 cache quantized per row,
+ * rows padded by 128 bytes when K % 2048 == 0).
+ *  x8       e4m3 codes [M, K], row stride K (from mq_quantize_e4m3 with
+ *           ldo = K), device, 16-byte aligned.
+ *  x_scale  f32 [M], device.
+ *  y        f32 [M, N].
+ * Same stream, workspace and split-K behaviour as mq_gemm.  Errors:
+ * MQ_ERR_INVALID, MQ_ERR_NO_CACHE (no e4m3 copy), MQ_ERR_SHAPE,
+ * MQ_ERR_ALIGN, MQ_ERR_OOM (split-K workspace), MQ_ERR_CUDA.
+ */
+int mq_gemm_e4m3(const void *x8, const float *x_scale, mq_handle w, float *y, int64_t M, void *stream);
+
+/* The weight's e4m3 copy: row stride ldk8 (bytes), codes [N, ldk8] and
+ * scales [N] (NULL without MQ_REG_E4M3).  Any output may be NULL.
+ * Errors: MQ_ERR_INVALID. */
+int mq_weight_e4m3_info(mq_handle w, int64_t *ldk8, const void **codes, const float **scales);
 
 /*
  * mq_gemm_noalloc -- the cached GEMM (same result as mq_gemm, same

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libmq.so")
 MQ_TYPE_F32, MQ_TYPE_F16, MQ_TYPE_BF16 = 0, 1, 30
 MQ_TYPE_Q4_0, MQ_TYPE_Q5_0, MQ_TYPE_Q5_1, MQ_TYPE_Q8_0 = 2, 6, 7, 8
 MQ_TYPE_Q4_K, MQ_TYPE_Q5_K, MQ_TYPE_Q6_K = 12, 13, 14
-MQ_REG_NO_CACHE, MQ_REG_NO_KPAD, MQ_REG_KPAD = 0x1, 0x2, 0x4
+MQ_REG_NO_CACHE, MQ_REG_NO_KPAD, MQ_REG_KPAD, MQ_REG_E4M3 = 0x1, 0x2, 0x4, 0x8
 STATUS = {0: "MQ_OK", -1: "MQ_ERR_INVALID", -2: "MQ_ERR_UNSUPPORTED_TYPE", -3: "MQ_ERR_SHAPE",
           -4: "MQ_ERR_ALIGN", -5: "MQ_ERR_NO_CACHE", -6: "MQ_ERR_OOM", -7: "MQ_ERR_CUDA",
           -8: "MQ_ERR_DEVICE", -9: "MQ_ERR_NO_DEVICE"}
@@ -28,7 +28,7 @@ EXPORTS = ("mq_register_weight", "mq_release_weight", "mq_weight_info", "mq_dequ
            "mq_gemm_fused", "mq_gemm_auto", "mq_get_m_gate", "mq_set_m_gate", "mq_reserve_workspace",
            "mq_stream_status", "mq_launch_count", "mq_error_string", "mq_last_error_detail", "mq_version",
            "mq_trace_enable", "mq_trace_count", "mq_trace_read", "mq_gemm_noalloc", "mq_gemm_grouped",
-           "mq_gemm_scratch")
+           "mq_gemm_scratch", "mq_quantize_e4m3", "mq_gemm_e4m3", "mq_weight_e4m3_info")
 MQ_TRACE_GEMM_CACHED, MQ_TRACE_GEMM_FUSED, MQ_TRACE_DECODE = 1, 2, 3
 
 
@@ -56,6 +56,9 @@ def _load() -> ctypes.CDLL:
         "mq_gemm_auto": ([_P, _P, _P, _I64, _P], ctypes.c_int),
         "mq_gemm_noalloc": ([_P, _P, _P, _I64, _P], ctypes.c_int),
         "mq_gemm_scratch": ([_P, _P, _P, _I64, _P, _I64, _P], ctypes.c_int),
+        "mq_quantize_e4m3": ([_P, _I64, _I64, _I64, _P, _I64, _P, _P], ctypes.c_int),
+        "mq_gemm_e4m3": ([_P, _P, _P, _P, _I64, _P], ctypes.c_int),
+        "mq_weight_e4m3_info": ([_P, ctypes.POINTER(_I64), ctypes.POINTER(_P), ctypes.POINTER(_P)], ctypes.c_int),
         "mq_gemm_grouped": ([_P, ctypes.POINTER(_P), ctypes.c_int, ctypes.POINTER(_P), _I64, _P], ctypes.c_int),
         "mq_get_m_gate": ([], _I64),
         "mq_set_m_gate": ([_I64], ctypes.c_int),
@@ -135,6 +138,19 @@ class Weight:
             return None
         return _tensor_from_ptr(ptr, (n, ldk), torch.float16)
 
+    def e4m3_tensors(self):
+        """(codes uint8 [N, ldk8], scales float32 [N]) views of the e4m3 copy,
+        or None without MQ_REG_E4M3."""
+        import torch
+        ldk8, codes, scales = _I64(), _P(), _P()
+        _check(_lib().mq_weight_e4m3_info(self.handle, ctypes.byref(ldk8), ctypes.byref(codes), ctypes.byref(scales)),
+               "mq_weight_e4m3_info")
+        if not codes.value:
+            return None
+        n = self.info()[0]
+        return (_tensor_from_ptr(codes.value, (n, ldk8.value), torch.uint8),
+                _tensor_from_ptr(scales.value, (n,), torch.float32))
+
     def release(self) -> None:
         if self.handle:
             _check(_lib().mq_release_weight(self.handle), "mq_release_weight")
@@ -161,7 +177,7 @@ def _tensor_from_ptr(ptr: int, shape, dtype):
     nbytes *= torch.empty((), dtype=dtype).element_size()
     h = _Holder()
     h.__cuda_array_interface__ = {
-        "shape": tuple(shape), "typestr": {torch.float16: "<f2", torch.float32: "<f4"}[dtype],
+        "shape": tuple(shape), "typestr": {torch.float16: "<f2", torch.float32: "<f4", torch.uint8: "|u1"}[dtype],
         "data": (ptr, False), "version": 3, "strides": None,
     }
     return torch.as_tensor(h, device="cuda")
@@ -217,6 +233,19 @@ def mq_gemm_scratch(x, w: Weight, y, scratch, M: int | None = None, stream=None)
     nbytes = scratch.numel() * scratch.element_size()
     _check(_lib().mq_gemm_scratch(_ptr(x), w.handle, _ptr(y), M if M is not None else x.shape[0], _ptr(scratch),
                                   nbytes, _stream(stream)), "mq_gemm_scratch")
+
+
+def mq_quantize_e4m3(x, dst, scales, stream=None) -> None:
+    """Row-wise e4m3 quantization of f16 x [rows, K] into dst (uint8, [rows,
+    >= K]) and scales (float32 [rows])."""
+    rows, K = x.shape
+    _check(_lib().mq_quantize_e4m3(_ptr(x), rows, K, x.stride(0), _ptr(dst), dst.stride(0), _ptr(scales),
+                                   _stream(stream)), "mq_quantize_e4m3")
+
+
+def mq_gemm_e4m3(x8, x_scale, w: Weight, y, M: int | None = None, stream=None) -> None:
+    _check(_lib().mq_gemm_e4m3(_ptr(x8), _ptr(x_scale), w.handle, _ptr(y), M if M is not None else x8.shape[0],
+                               _stream(stream)), "mq_gemm_e4m3")
 
 
 def mq_get_m_gate() -> int:

@@ -19,7 +19,7 @@ LIB = os.path.join(PKG, "libmq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               f"-I{os.path.join(ROOT, 'include')}", f"-I{CSRC}"]
-SOURCES = ["api.cpp", "dequant.cu", "gemm.cu", "fused.cu", "noalloc.cu"]
+SOURCES = ["api.cpp", "dequant.cu", "gemm.cu", "fused.cu", "noalloc.cu", "quant8.cu"]
 
 
 def nvcc() -> str:

@@ -34,6 +34,10 @@ struct mq_weight {
     CUtensorMap tm_cache;
     int raw_g;           // > 0: the fused path reads raw blocks through raw_maps
     mq::RawMaps raw_maps;
+    uint8_t *w8;         // MQ_REG_E4M3: e4m3 codes [N, ldk8], else null
+    float *w8_scale;     // MQ_REG_E4M3: one scale per row [N]
+    int64_t ldk8;
+    CUtensorMap tm_w8;
 };
 
 namespace {
@@ -380,8 +384,10 @@ typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32
                                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-CUresult encode_f16_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
-                       int box_rows)
+namespace {
+
+CUresult encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, int esize, const void *base, int64_t rows,
+                   int64_t cols, int64_t ld, int box_cols, int box_rows)
 {
     static PFN_encodeTiled fn = nullptr;
     if (!fn) {
@@ -394,12 +400,25 @@ CUresult encode_f16_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t
         fn = reinterpret_cast<PFN_encodeTiled>(p);
     }
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+CUresult encode_f16_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                       int box_rows)
+{
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, rows, cols, ld, box_cols, box_rows);
+}
+
+CUresult encode_u8_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                      int box_rows)
+{
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, ld, box_cols, box_rows);
 }
 
 int set_error(int code, const char *what, cudaError_t e)
@@ -515,7 +534,7 @@ int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, ui
     if (!block_format(type, qk, bb))
         return fail(MQ_ERR_UNSUPPORTED_TYPE, "type id %d is not supported (supported: %s); the weight has no kernel",
                     (int)type, kTypeList);
-    if (flags & ~(MQ_REG_NO_CACHE | MQ_REG_NO_KPAD | MQ_REG_KPAD))
+    if (flags & ~(MQ_REG_NO_CACHE | MQ_REG_NO_KPAD | MQ_REG_KPAD | MQ_REG_E4M3))
         return fail(MQ_ERR_INVALID, "unknown flag bits 0x%x", flags);
     if ((flags & MQ_REG_NO_KPAD) && (flags & MQ_REG_KPAD))
         return fail(MQ_ERR_INVALID, "MQ_REG_NO_KPAD and MQ_REG_KPAD are exclusive");
@@ -529,6 +548,9 @@ int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, ui
         return fail(MQ_ERR_SHAPE, "N*K=%lld is not a whole number of %d-element blocks", (long long)(N * K), qk);
     if (!aligned16(qdata))
         return fail(MQ_ERR_ALIGN, "qdata=%p is not 16-byte aligned", qdata);
+    if ((flags & MQ_REG_E4M3) && ((flags & MQ_REG_NO_CACHE) || K % 16 != 0))
+        return fail(MQ_ERR_INVALID, "MQ_REG_E4M3 quantizes the f16 cache: it needs the cache (no MQ_REG_NO_CACHE) "
+                                    "and K %% 16 == 0 (K=%lld)", (long long)K);
     if ((flags & MQ_REG_NO_CACHE) && (type == MQ_TYPE_F32 || type == MQ_TYPE_BF16))
         return fail(MQ_ERR_INVALID, "type %d: an F32 or BF16 weight is read through its f16 copy; MQ_REG_NO_CACHE "
                                     "applies to block formats and F16", (int)type);
@@ -563,6 +585,9 @@ int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, ui
     w->qdata = static_cast<const uint8_t *>(qdata);
     w->cache = nullptr;
     w->cache_owned = false;
+    w->w8 = nullptr;
+    w->w8_scale = nullptr;
+    w->ldk8 = 0;
     w->device = dev;
     w->raw_g = env_int("MQ_RAW_TMA", 1) ? mq::encode_raw_maps(&w->raw_maps, qdata, type, N, K) : 0;
 
@@ -609,9 +634,57 @@ int mq_register_weight(mq_type type, const void *qdata, int64_t N, int64_t K, ui
             return fail(MQ_ERR_CUDA, "tensor map for the f16 cache: CUresult %d", (int)cr);
         }
     }
+    if (flags & MQ_REG_E4M3) {
+        // The 8-bit copy: each cache row quantized to e4m3 with its own
+        // scale; rows padded by one 128-byte line when they are a multiple
+        // of 2048 bytes (the cache's rule, in bytes).
+        int64_t ldk8 = (K % 2048 == 0) ? K + 128 : K;
+        if (flags & MQ_REG_KPAD)
+            ldk8 = K + 128;
+        else if (flags & MQ_REG_NO_KPAD)
+            ldk8 = K;
+        void *p8 = nullptr, *ps = nullptr;
+        cudaError_t e = cudaMalloc(&p8, static_cast<size_t>(N) * static_cast<size_t>(ldk8));
+        if (e == cudaSuccess)
+            e = cudaMalloc(&ps, static_cast<size_t>(N) * sizeof(float));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(p8);
+            if (w->cache_owned) {
+                cudaStreamSynchronize(s);
+                cudaFree(w->cache);
+            }
+            delete w;
+            return fail(MQ_ERR_OOM, "e4m3 copy of %lld x %lld bytes: %s", (long long)N, (long long)ldk8,
+                        cudaGetErrorString(e));
+        }
+        w->w8 = static_cast<uint8_t *>(p8);
+        w->w8_scale = static_cast<float *>(ps);
+        w->ldk8 = ldk8;
+        const int64_t tr = trace_begin(s, MQ_TRACE_DECODE, type, 0, N, K);
+        e = mq::launch_quant_e4m3(w->cache, N, K, w->ldk, w->w8, ldk8, w->w8_scale, s);
+        trace_mark(tr, 1, s);
+        trace_mark(tr, 2, s);
+        if (e == cudaSuccess && ldk8 > K)
+            e = cudaMemset2DAsync(w->w8 + K, static_cast<size_t>(ldk8), 0, static_cast<size_t>(ldk8 - K),
+                                  static_cast<size_t>(N), s);
+        CUresult cr = CUDA_SUCCESS;
+        if (e == cudaSuccess)
+            cr = mq::encode_u8_2d(&w->tm_w8, w->w8, N, K, ldk8, 128, 128);
+        if (e != cudaSuccess || cr != CUDA_SUCCESS) {
+            cudaStreamSynchronize(s);
+            cudaFree(w->w8);
+            cudaFree(w->w8_scale);
+            if (w->cache_owned)
+                cudaFree(w->cache);
+            delete w;
+            return e != cudaSuccess ? cuda_fail(e, "e4m3 quantization of the cache")
+                                    : fail(MQ_ERR_CUDA, "tensor map for the e4m3 copy: CUresult %d", (int)cr);
+        }
+    }
     if (log_on())
-        fprintf(stderr, "[mq] register type=%d N=%lld K=%lld ldk=%lld cache=%s\n", (int)type, (long long)N,
-                (long long)K, (long long)ldk, w->cache ? "yes" : "no");
+        fprintf(stderr, "[mq] register type=%d N=%lld K=%lld ldk=%lld cache=%s e4m3=%s\n", (int)type, (long long)N,
+                (long long)K, (long long)ldk, w->cache ? "yes" : "no", w->w8 ? "yes" : "no");
     {
         std::lock_guard<std::mutex> lk(g_mu);
         g_live.insert(w);
@@ -628,12 +701,15 @@ int mq_release_weight(mq_handle w)
             return fail(MQ_ERR_INVALID, "handle %p is not a live registered weight", (void *)w);
         g_live.erase(w);
     }
-    if (w->cache && w->cache_owned) {
+    if ((w->cache && w->cache_owned) || w->w8) {
         int cur = 0;
         cudaGetDevice(&cur);
         cudaSetDevice(w->device);
         cudaDeviceSynchronize();
-        cudaFree(w->cache);
+        if (w->cache_owned)
+            cudaFree(w->cache);
+        cudaFree(w->w8);
+        cudaFree(w->w8_scale);
         cudaSetDevice(cur);
     }
     delete w;
@@ -783,6 +859,110 @@ int mq_gemm_scratch(const void *x, mq_handle w, float *y, int64_t M, void *scrat
     trace_mark(tr, 1, s);
     trace_mark(tr, 2, s);
     return run_gemm(x, &tmp, y, M, s, false);
+}
+
+int mq_weight_e4m3_info(mq_handle w, int64_t *ldk8, const void **codes, const float **scales)
+{
+    int rc = check_handle(w);
+    if (rc)
+        return rc;
+    if (ldk8) *ldk8 = w->ldk8;
+    if (codes) *codes = w->w8;
+    if (scales) *scales = w->w8_scale;
+    return MQ_OK;
+}
+
+int mq_quantize_e4m3(const void *x, int64_t rows, int64_t K, int64_t ld, void *dst, int64_t ldo, float *scales,
+                     void *stream)
+{
+    if (!x || !dst || !scales)
+        return fail(MQ_ERR_INVALID, "%s is NULL", !x ? "x" : (!dst ? "dst" : "scales"));
+    if (rows < 1 || K < 16 || K % 16 != 0 || ld < K || ld % 8 != 0 || ldo < K || ldo % 16 != 0)
+        return fail(MQ_ERR_SHAPE,
+                    "rows=%lld K=%lld ld=%lld ldo=%lld: need rows >= 1, K %% 16 == 0, ld >= K, ld %% 8 == 0, "
+                    "ldo >= K, ldo %% 16 == 0",
+                    (long long)rows, (long long)K, (long long)ld, (long long)ldo);
+    if (!aligned16(x) || !aligned16(dst) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+        return fail(MQ_ERR_ALIGN, "x and dst must be 16-byte aligned, scales 4-byte aligned");
+    DevState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc)
+        return rc;
+    cudaError_t e = mq::launch_quant_e4m3(static_cast<const __half *>(x), rows, K, ld, static_cast<uint8_t *>(dst),
+                                          ldo, scales, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "e4m3 quantization launch");
+    return MQ_OK;
+}
+
+int mq_gemm_e4m3(const void *x8, const float *x_scale, mq_handle w, float *y, int64_t M, void *stream)
+{
+    int rc = check_gemm_args(x8, w, y, M);
+    if (rc)
+        return rc;
+    if (!x_scale)
+        return fail(MQ_ERR_INVALID, "x_scale is NULL");
+    if (!w->w8)
+        return fail(MQ_ERR_NO_CACHE, "weight was registered without MQ_REG_E4M3: it has no e4m3 copy");
+    DevState *d = nullptr;
+    rc = device_state(&d);
+    if (rc)
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool splitk_on = env_int("MQ_SPLITK", 1) != 0;
+    const int64_t want = splitk_on ? mq::plan_ws_bytes_wanted(M, w->N, w->K, d->sms, false, 0, mq::kKStepE4m3) : 0;
+    if (want > d->ws_bytes) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(s, &cs);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaStreamIsCapturing");
+        if (cs == cudaStreamCaptureStatusNone) {
+            std::lock_guard<std::mutex> lk(g_mu);
+            rc = grow_workspace(*d, want);
+            if (rc)
+                return rc;
+        }
+    }
+    const mq::GemmPlan plan = mq::plan_gemm(M, w->N, w->K, d->sms, false, splitk_on ? d->ws_bytes : 0, 0, mq::kKStepE4m3);
+    CUtensorMap tm_x;
+    CUresult cr = mq::encode_u8_2d(&tm_x, x8, M, w->K, w->K, 128, plan.bn);
+    if (cr != CUDA_SUCCESS)
+        return fail(MQ_ERR_CUDA, "tensor map for x8 (M=%lld, K=%lld): CUresult %d", (long long)M, (long long)w->K,
+                    (int)cr);
+    mq::GemmArgs a{};
+    a.y = y;
+    a.ws = d->ws;
+    a.status = d->status;
+    a.M = M;
+    a.N = w->N;
+    a.K = w->K;
+    a.m_tiles = static_cast<int>((M + plan.bn - 1) / plan.bn);
+    a.n_tiles = static_cast<int>((w->N + 127) / 128);
+    a.kblocks = static_cast<int>((w->K + mq::kKStepE4m3 - 1) / mq::kKStepE4m3);
+    a.full_tiles = plan.full_tiles;
+    a.split = plan.split;
+    a.units = plan.units;
+    a.kb_align = plan.kb_align;
+    a.qtype = w->type;
+    a.x_scale = x_scale;
+    a.groups = 1;
+    a.g_tile0[0] = 0;
+    a.g_tile0[1] = a.n_tiles;
+    a.g_y[0] = y;
+    a.g_N[0] = w->N;
+    a.g_wscale[0] = w->w8_scale;
+    mq::WMaps maps{};
+    maps.m[0] = w->tm_w8;
+    const int64_t tr = trace_begin(s, MQ_TRACE_GEMM_CACHED, w->type, M, w->N, w->K);
+    cudaError_t e = mq::launch_gemm_e4m3(maps, tm_x, a, plan, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "e4m3 GEMM launch");
+    trace_mark(tr, 1, s);
+    e = mq::launch_splitk_reduce(a, plan, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "split-K reduce launch");
+    trace_mark(tr, 2, s, plan.split > 1 && plan.tiles > plan.full_tiles);
+    return MQ_OK;
 }
 
 int64_t mq_get_m_gate(void) { return current_gate(); }

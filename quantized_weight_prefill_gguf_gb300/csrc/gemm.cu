@@ -27,6 +27,12 @@
 //    let the epilogue of tile i overlap the main loop of tile i+1.
 //  * Every pipeline wait is bounded (mq_ptx.cuh); on a timeout all roles stop
 //    and the CTA still frees its TMEM.
+//
+// The 8-bit variant (k_gemm_e4m3) is the same kernel on e4m3 operands: a
+// stage is still one 128-byte swizzle row per operand row, now 128 K
+// elements, and each of its four MMAs (kind::f8f6f4, K = 32) advances 32
+// bytes as for f16; the epilogue scales by the weight row's and the token's
+// quantization scales.
 #include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -49,11 +55,13 @@ template <int BN> struct Cfg {
     static constexpr int kSmem = 1024 + kStages * (kABytes + kBBytes) + 256;
 };
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_cached(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
+// The kernel body: F8 selects e4m3 operands (K step kBK8, kind::f8f6f4,
+// scaled epilogue) over f16 (K step kBK, kind::f16).
+template <int BN, bool F8>
+__device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &tm_x, const GemmArgs &a)
 {
     using C = Cfg<BN>;
+    constexpr int kStep = F8 ? kBK8 : kBK;   // K elements per stage (128 bytes per row either way)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = base;
@@ -114,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n0 = (nt - a.g_tile0[g]) * kTileRows;
                 for (int kb = ui.kb0; kb < ui.kb1 && pre < C::kStages; ++kb, ++pre) {
                     mbar_arrive_expect_tx(&full[pre], kABytes + C::kBBytes);
-                    tma_load_2d(sA + pre * kABytes, &tm_w.m[g], &full[pre], kb * kBK, n0);
+                    tma_load_2d(sA + pre * kABytes, &tm_w.m[g], &full[pre], kb * kStep, n0);
                     issued |= 1u << pre;
                 }
             }
@@ -130,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = ui.kb0; kb < ui.kb1; ++kb, ++step) {
                     if (step < pre) {
                         // weight tile already requested (stage == step, phase 0)
-                        tma_load_2d(sB + stage * C::kBBytes, &tm_x, &full[stage], kb * kBK, m0);
+                        tma_load_2d(sB + stage * C::kBBytes, &tm_x, &full[stage], kb * kStep, m0);
                         if (++stage == C::kStages) {
                             stage = 0;
                             phase ^= 1u;
@@ -142,8 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full[stage], kABytes + C::kBBytes);
-                    tma_load_2d(sA + stage * kABytes, tmw, &full[stage], kb * kBK, n0);
-                    tma_load_2d(sB + stage * C::kBBytes, &tm_x, &full[stage], kb * kBK, m0);
+                    tma_load_2d(sA + stage * kABytes, tmw, &full[stage], kb * kStep, n0);
+                    tma_load_2d(sB + stage * C::kBBytes, &tm_x, &full[stage], kb * kStep, m0);
                     issued |= 1u << stage;
                     issue_parity = (issue_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) {
@@ -167,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // only adds sit between consecutive MMAs of a stage.  (Waiting
             // for the next stage before the current stage's last MMA was
             // measured slower: it delays the commit that frees the stage.)
-            constexpr uint32_t idesc = idesc_f16_f32(kTileRows, BN);
+            constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(kTileRows, BN) : idesc_f16_f32(kTileRows, BN);
             const uint64_t a_desc0 = sdesc_k_sw128(smem_u32(sA));
             const uint64_t b_desc0 = sdesc_k_sw128(smem_u32(sB));
             int stage = 0;
@@ -193,8 +201,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * kABytes) >> 4);
                     const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * C::kBBytes) >> 4);
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)
-                        umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > ui.kb0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k) {   // four MMAs of 32 bytes of K each
+                        if constexpr (F8)
+                            umma_e4m3(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > ui.kb0 || k > 0) ? 1u : 0u);
+                        else
+                            umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > ui.kb0 || k > 0) ? 1u : 0u);
+                    }
                     umma_commit(&empty[stage]);
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -217,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue: warps 2..5 own TMEM lane quarters 2,3,0,1
-        epilogue_role<BN>(a, tmem, tfull, tempty, abort_flag, warp, lane);
+        epilogue_role<BN, 2, 1, F8>(a, tmem, tfull, tempty, abort_flag, warp, lane);
     }
 
     tc_fence_before();
@@ -226,6 +238,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_cached(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
+{
+    gemm_body<BN, false>(tm_w, tm_x, a);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_e4m3(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
+{
+    gemm_body<BN, true>(tm_w, tm_x, a);
 }
 
 // Fixed-order split-K reduction: Y = sum over p = 0..split-1 of the partial
@@ -277,30 +303,32 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(const GemmArgs a, int bn)
     }
 }
 
-template <int BN>
+template <int BN, bool F8>
 cudaError_t launch_bn(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p, cudaStream_t s)
 {
     using C = Cfg<BN>;
-    static bool attr_done[64] = {};   // the attribute is set once per device
+    auto *kern = F8 ? k_gemm_e4m3<BN> : k_gemm_cached<BN>;
+    static bool attr_done[64] = {};   // the attribute is set once per device (per instantiation)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(k_gemm_cached<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess)
             return e;
         if (dev >= 0 && dev < 64)
             attr_done[dev] = true;
     }
-    e = launch_kernel(k_gemm_cached<BN>, dim3(p.grid), dim3(kThreads), C::kSmem, s, tw, tx, a);
+    e = launch_kernel(kern, dim3(p.grid), dim3(kThreads), C::kSmem, s, tw, tx, a);
     note_launch();
     return e;
 }
 
 }  // namespace
 
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available, int bn_override)
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available, int bn_override,
+                   int kstep)
 {
     GemmPlan p{};
     // The fused path keeps a whole 256-element K chunk of activations per
@@ -317,7 +345,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t
     p.kb_align = fused ? 4 : 1;
     const int64_t m_tiles = (M + p.bn - 1) / p.bn;
     const int64_t n_tiles = (N + kTileRows - 1) / kTileRows;
-    const int64_t kblocks = (K + kBK - 1) / kBK;
+    const int64_t kblocks = (K + kstep - 1) / kstep;
     const int64_t groups = (kblocks + p.kb_align - 1) / p.kb_align;
     p.tiles = static_cast<int>(m_tiles * n_tiles);
     p.split = 1;
@@ -344,19 +372,31 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t
     return p;
 }
 
-int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused, int bn_override)
+int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused, int bn_override, int kstep)
 {
-    return plan_gemm(M, N, K, sms, fused, INT64_MAX, bn_override).ws_bytes;
+    return plan_gemm(M, N, K, sms, fused, INT64_MAX, bn_override, kstep).ws_bytes;
 }
 
 cudaError_t launch_gemm_cached(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p,
                                cudaStream_t s)
 {
     switch (p.bn) {
-    case 256: return launch_bn<256>(tw, tx, a, p, s);
-    case 128: return launch_bn<128>(tw, tx, a, p, s);
-    case 64: return launch_bn<64>(tw, tx, a, p, s);
-    case 32: return launch_bn<32>(tw, tx, a, p, s);
+    case 256: return launch_bn<256, false>(tw, tx, a, p, s);
+    case 128: return launch_bn<128, false>(tw, tx, a, p, s);
+    case 64: return launch_bn<64, false>(tw, tx, a, p, s);
+    case 32: return launch_bn<32, false>(tw, tx, a, p, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gemm_e4m3(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p,
+                             cudaStream_t s)
+{
+    switch (p.bn) {
+    case 256: return launch_bn<256, true>(tw, tx, a, p, s);
+    case 128: return launch_bn<128, true>(tw, tx, a, p, s);
+    case 64: return launch_bn<64, true>(tw, tx, a, p, s);
+    case 32: return launch_bn<32, true>(tw, tx, a, p, s);
     default: return cudaErrorInvalidValue;
     }
 }

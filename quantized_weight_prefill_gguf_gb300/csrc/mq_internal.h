@@ -31,6 +31,9 @@ cudaError_t launch_dequant(int type, const void *q, int64_t nblocks, __half *out
 // A single weight is the group of one (g_y[0] = y, g_N[0] = N).
 constexpr int kMaxGroup = 4;
 
+// K elements per pipeline stage of the 8-bit (e4m3) GEMM: one 128-byte row.
+constexpr int kKStepE4m3 = 128;
+
 struct GemmArgs {
     float *y;            // [M, N] f32 output
     float *ws;           // split-K partial planes: [slot][part][BN][128]
@@ -52,6 +55,8 @@ struct GemmArgs {
     int64_t raw_rb;      // fused path: bytes per weight row (when rows start on block boundaries)
     int stall_producer;  // failure-injection hook: the weight producer issues nothing, so the
                          // consumers' bounded waits run out (tests of the timeout path)
+    const float *x_scale;           // 8-bit path: per-token scale of X [M]
+    const float *g_wscale[kMaxGroup];  // 8-bit path: per-row scale of each member's weight
     int groups;                     // members of the group (1 for a single weight)
     int g_tile0[kMaxGroup + 1];     // first n-tile of each member; g_tile0[groups] = n_tiles
     float *g_y[kMaxGroup];          // member outputs
@@ -96,16 +101,30 @@ struct GemmPlan {
 
 // Choose tile width, split-K and grid for an M x N x K problem on `sms` SMs.
 // bn_override > 0 forces the cached path's tile width (32, 64, 128 or 256).
+// kstep: K elements per pipeline stage (64 for f16 operands, 128 for 8-bit).
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available,
-                   int bn_override = 0);
+                   int bn_override = 0, int kstep = 64);
 
 // Workspace bytes the plan would use with an unlimited workspace.
-int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused, int bn_override = 0);
+int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused, int bn_override = 0,
+                             int kstep = 64);
 
 // Cached path: tm_w.m[g] maps member g's f16 cache [N_g, ldk_g] (box 64 x
 // 128), tm_x maps X [M, K] (box 64 x bn).  All 128-byte swizzled.
 cudaError_t launch_gemm_cached(const WMaps &tm_w, const CUtensorMap &tm_x, const GemmArgs &a,
                                const GemmPlan &p, cudaStream_t s);
+
+// 8-bit path: the same GEMM on e4m3 operands (tm_w.m[g] maps member g's
+// e4m3 copy [N_g, ldk8_g], box 128 x 128; tm_x maps X8 [M, K], box 128 x
+// bn; 128-byte swizzle), Y = acc * g_wscale[g][n] * x_scale[m].
+cudaError_t launch_gemm_e4m3(const WMaps &tm_w, const CUtensorMap &tm_x, const GemmArgs &a,
+                             const GemmPlan &p, cudaStream_t s);
+
+// Row-wise e4m3 quantization of an f16 matrix [rows, K] (row stride ld):
+// codes into dst (row stride ldo bytes) and one f32 scale per row.
+// K % 16 == 0, ld % 8 == 0, ldo % 16 == 0.
+cudaError_t launch_quant_e4m3(const __half *src, int64_t rows, int64_t K, int64_t ld, uint8_t *dst, int64_t ldo,
+                              float *scales, cudaStream_t s);
 
 // Fused path: tm_x as above; the weight is read from a.wq, through `maps`
 // when a.raw_g > 0.
@@ -138,5 +157,9 @@ unsigned noalloc_take_status();
 // elements, a box of box_cols x box_rows and 128-byte swizzle.
 CUresult encode_f16_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld,
                        int box_cols, int box_rows);
+
+// The same for a byte matrix (e4m3 codes): ld in bytes.
+CUresult encode_u8_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld,
+                      int box_cols, int box_rows);
 
 }  // namespace mq

@@ -220,6 +220,20 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T on e4m3 operands (kind::f8f6f4, K = 32
+// per instruction, the same 32 bytes of a 128-byte swizzle row as K = 16
+// of f16), f32 accumulation.
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T: the A operand (M = 128 rows) is read from
 // tensor memory, one row per lane, two f16 per 32-bit column (K index 2c in
 // the low half of column c, 2c+1 in the high half), 8 columns per K = 16.
@@ -322,6 +336,23 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N)
 {
     return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0u << 16) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f8f6f4 with A and B e4m3 (format code 0
+// in bits 7-9 and 10-12), K-major, D f32: the same fields as above.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
+{
+    return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0u << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Two binary32 values to two e4m3 codes (round to nearest even, finite
+// values past 448 clamped): lo in bits 0-7, hi in bits 8-15.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // 16-byte read-only global load that bypasses L1.

@@ -11,6 +11,7 @@
 namespace mq {
 
 constexpr int kBK = 64;                       // K elements per MMA stage (one 128-byte swizzle row of f16)
+constexpr int kBK8 = kKStepE4m3;              // the same 128-byte row of 8-bit operands
 constexpr int kTileRows = 128;                // weight rows per tile (the MMA's M)
 constexpr int kABytes = kTileRows * kBK * 2;  // 16 KB f16 weight tile per stage
 
@@ -59,7 +60,11 @@ __device__ __forceinline__ UnitInfo unit_info(const GemmArgs &a, int u)
 // take kb_split of every kb_split*NPART consecutive K steps; part 1 exists
 // when the unit has more than kb_split K steps, and the parts are added
 // here in part order (0 + 1).
-template <int BN, int NACC = 2, int NPART = 1>
+//
+// SCALED (the 8-bit path): every accumulator value is multiplied by its
+// weight row's scale and then by its token's scale, RN32(RN32(acc * sw) *
+// sx), before it is stored (partial planes too: the scaling is linear).
+template <int BN, int NACC = 2, int NPART = 1, bool SCALED = false>
 __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, uint64_t *tfull, uint64_t *tempty,
                                               volatile int *abort_flag, int warp, int lane, int kb_split = 1)
 {
@@ -79,6 +84,9 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
         const int64_t n = static_cast<int64_t>(nt - a.g_tile0[g]) * kTileRows + row;   // row inside member g
         const int64_t m0 = static_cast<int64_t>(ui.tile % a.m_tiles) * BN;
         const bool two = NPART == 2 && ui.kb1 - ui.kb0 > kb_split;
+        float wscale = 0.0f;
+        if constexpr (SCALED)
+            wscale = n < Ng ? a.g_wscale[g][n] : 0.0f;
         constexpr int kCols = BN < 32 ? BN : 32;   // columns per TMEM load
 #pragma unroll 1
         for (int c = 0; c < BN; c += kCols) {
@@ -107,6 +115,16 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
                 }
             }
             tmem_ld_wait();
+            if constexpr (SCALED) {
+                // lane j fetches token m0+c+j's scale; every lane takes it by shuffle
+                const int64_t mj = m0 + c + lane;
+                const float xs_lane = (lane < kCols && mj < a.M) ? a.x_scale[mj] : 0.0f;
+#pragma unroll
+                for (int j = 0; j < kCols; ++j) {
+                    const float xs = __shfl_sync(0xFFFFFFFFu, xs_lane, j);
+                    r[j] = __float_as_uint(__fmul_rn(__fmul_rn(__uint_as_float(r[j]), wscale), xs));
+                }
+            }
             if (ui.part < 0) {
                 if (n < Ng) {
                     float *yp = a.g_y[g] + (m0 + c) * Ng + n;
