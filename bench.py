@@ -637,7 +637,7 @@ def row_pad(mq, torch, stream):
 def e4m3_layer(mq, torch, stream, weights, qdev, xdev, ys_f16, P, steps, flops_step):
     """The layer step on the 8-bit variant: per step the activations of the
     four launch groups (q|k|v, o, gate|up, down) are quantized once each and
-    the seven GEMMs run on e4m3 operands.  Timed like the main loop (CUDA
+    the seven GEMMs run on e4m3 operands, grouped as in the f16 step.  Timed like the main loop (CUDA
     events around `steps` steps after 5 warm-ups); the e4m3 kernel's mean
     launch time comes from a traced pass."""
     M = M_TOKENS
@@ -656,9 +656,11 @@ def e4m3_layer(mq, torch, stream, weights, qdev, xdev, ys_f16, P, steps, flops_s
             K = weights[idx[g[0]]].K
             q8, sx = x8[g]
             mq.mq_quantize_e4m3(xdev[K][:M], q8, sx, stream)
-            for name in g:
-                i = idx[name]
-                mq.mq_gemm_e4m3(q8, sx, hs[i], ys[i], M, stream)
+            members = [idx[name] for name in g]
+            if len(members) == 1:
+                mq.mq_gemm_e4m3(q8, sx, hs[members[0]], ys[members[0]], M, stream)
+            else:
+                mq.mq_gemm_e4m3_grouped(q8, sx, [hs[i] for i in members], [ys[i] for i in members], M, stream)
 
     for _ in range(5):
         step()

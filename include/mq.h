@@ -283,6 +283,13 @@ int mq_quantize_e4m3(const void *x, int64_t rows, int64_t K, int64_t ld, void *d
  */
 int mq_gemm_e4m3(const void *x8, const float *x_scale, mq_handle w, float *y, int64_t M, void *stream);
 
+/* mq_gemm_e4m3 for `count` (1..4) weights sharing K and the quantized X:
+ * y[g] = the member-g product, one launch when every N is a multiple of 128
+ * (else one after another), as mq_gemm_grouped.  Errors: those of
+ * mq_gemm_grouped, MQ_ERR_NO_CACHE for a member without an e4m3 copy. */
+int mq_gemm_e4m3_grouped(const void *x8, const float *x_scale, const mq_handle *w, int count, float *const *y,
+                         int64_t M, void *stream);
+
 /* The weight's e4m3 copy: row stride ldk8 (bytes), codes [N, ldk8] and
  * scales [N] (NULL without MQ_REG_E4M3).  Any output may be NULL.
  * Errors: MQ_ERR_INVALID. */

@@ -28,7 +28,8 @@ EXPORTS = ("mq_register_weight", "mq_release_weight", "mq_weight_info", "mq_dequ
            "mq_gemm_fused", "mq_gemm_auto", "mq_get_m_gate", "mq_set_m_gate", "mq_reserve_workspace",
            "mq_stream_status", "mq_launch_count", "mq_error_string", "mq_last_error_detail", "mq_version",
            "mq_trace_enable", "mq_trace_count", "mq_trace_read", "mq_gemm_noalloc", "mq_gemm_grouped",
-           "mq_gemm_scratch", "mq_quantize_e4m3", "mq_gemm_e4m3", "mq_weight_e4m3_info")
+           "mq_gemm_scratch", "mq_quantize_e4m3", "mq_gemm_e4m3", "mq_weight_e4m3_info",
+           "mq_gemm_e4m3_grouped")
 MQ_TRACE_GEMM_CACHED, MQ_TRACE_GEMM_FUSED, MQ_TRACE_DECODE = 1, 2, 3
 
 
@@ -58,6 +59,8 @@ def _load() -> ctypes.CDLL:
         "mq_gemm_scratch": ([_P, _P, _P, _I64, _P, _I64, _P], ctypes.c_int),
         "mq_quantize_e4m3": ([_P, _I64, _I64, _I64, _P, _I64, _P, _P], ctypes.c_int),
         "mq_gemm_e4m3": ([_P, _P, _P, _P, _I64, _P], ctypes.c_int),
+        "mq_gemm_e4m3_grouped": ([_P, _P, ctypes.POINTER(_P), ctypes.c_int, ctypes.POINTER(_P), _I64, _P],
+                                 ctypes.c_int),
         "mq_weight_e4m3_info": ([_P, ctypes.POINTER(_I64), ctypes.POINTER(_P), ctypes.POINTER(_P)], ctypes.c_int),
         "mq_gemm_grouped": ([_P, ctypes.POINTER(_P), ctypes.c_int, ctypes.POINTER(_P), _I64, _P], ctypes.c_int),
         "mq_get_m_gate": ([], _I64),
@@ -246,6 +249,17 @@ def mq_quantize_e4m3(x, dst, scales, stream=None) -> None:
 def mq_gemm_e4m3(x8, x_scale, w: Weight, y, M: int | None = None, stream=None) -> None:
     _check(_lib().mq_gemm_e4m3(_ptr(x8), _ptr(x_scale), w.handle, _ptr(y), M if M is not None else x8.shape[0],
                                _stream(stream)), "mq_gemm_e4m3")
+
+
+def mq_gemm_e4m3_grouped(x8, x_scale, ws, ys, M: int | None = None, stream=None) -> None:
+    """One e4m3 GEMM launch for weights sharing K and the quantized X."""
+    if len(ws) != len(ys):
+        raise ValueError(f"{len(ws)} weights but {len(ys)} outputs")
+    n = len(ws)
+    harr = (_P * n)(*[w.handle for w in ws])
+    yarr = (_P * n)(*[_ptr(y) for y in ys])
+    _check(_lib().mq_gemm_e4m3_grouped(_ptr(x8), _ptr(x_scale), harr, n, yarr, M if M is not None else x8.shape[0],
+                                       _stream(stream)), "mq_gemm_e4m3_grouped")
 
 
 def mq_get_m_gate() -> int:

@@ -895,22 +895,25 @@ int mq_quantize_e4m3(const void *x, int64_t rows, int64_t K, int64_t ld, void *d
     return MQ_OK;
 }
 
-int mq_gemm_e4m3(const void *x8, const float *x_scale, mq_handle w, float *y, int64_t M, void *stream)
+namespace {
+
+// Plan, workspace and launch of one e4m3 GEMM launch: one weight, or a group
+// of weights sharing K and the quantized X (every member's N a multiple of
+// 128), stacked along N as in run_gemm_group.
+int run_e4m3_group(const void *x8, const float *x_scale, const mq_handle *ws, float *const *ys, int count, int64_t M,
+                   cudaStream_t s)
 {
-    int rc = check_gemm_args(x8, w, y, M);
-    if (rc)
-        return rc;
-    if (!x_scale)
-        return fail(MQ_ERR_INVALID, "x_scale is NULL");
-    if (!w->w8)
-        return fail(MQ_ERR_NO_CACHE, "weight was registered without MQ_REG_E4M3: it has no e4m3 copy");
     DevState *d = nullptr;
-    rc = device_state(&d);
+    int rc = device_state(&d);
     if (rc)
         return rc;
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const mq_handle w = ws[0];
+    int64_t n_total = 0;
+    for (int g = 0; g < count; ++g)
+        n_total += ws[g]->N;
     const bool splitk_on = env_int("MQ_SPLITK", 1) != 0;
-    const int64_t want = splitk_on ? mq::plan_ws_bytes_wanted(M, w->N, w->K, d->sms, false, 0, mq::kKStepE4m3) : 0;
+    const int64_t want =
+        splitk_on ? mq::plan_ws_bytes_wanted(M, n_total, w->K, d->sms, false, 0, mq::kKStepE4m3) : 0;
     if (want > d->ws_bytes) {
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         cudaError_t e = cudaStreamIsCapturing(s, &cs);
@@ -923,21 +926,21 @@ int mq_gemm_e4m3(const void *x8, const float *x_scale, mq_handle w, float *y, in
                 return rc;
         }
     }
-    const mq::GemmPlan plan = mq::plan_gemm(M, w->N, w->K, d->sms, false, splitk_on ? d->ws_bytes : 0, 0, mq::kKStepE4m3);
+    const mq::GemmPlan plan =
+        mq::plan_gemm(M, n_total, w->K, d->sms, false, splitk_on ? d->ws_bytes : 0, 0, mq::kKStepE4m3);
     CUtensorMap tm_x;
     CUresult cr = mq::encode_u8_2d(&tm_x, x8, M, w->K, w->K, 128, plan.bn);
     if (cr != CUDA_SUCCESS)
         return fail(MQ_ERR_CUDA, "tensor map for x8 (M=%lld, K=%lld): CUresult %d", (long long)M, (long long)w->K,
                     (int)cr);
     mq::GemmArgs a{};
-    a.y = y;
+    a.y = ys[0];
     a.ws = d->ws;
     a.status = d->status;
     a.M = M;
-    a.N = w->N;
+    a.N = n_total;
     a.K = w->K;
     a.m_tiles = static_cast<int>((M + plan.bn - 1) / plan.bn);
-    a.n_tiles = static_cast<int>((w->N + 127) / 128);
     a.kblocks = static_cast<int>((w->K + mq::kKStepE4m3 - 1) / mq::kKStepE4m3);
     a.full_tiles = plan.full_tiles;
     a.split = plan.split;
@@ -945,15 +948,20 @@ int mq_gemm_e4m3(const void *x8, const float *x_scale, mq_handle w, float *y, in
     a.kb_align = plan.kb_align;
     a.qtype = w->type;
     a.x_scale = x_scale;
-    a.groups = 1;
-    a.g_tile0[0] = 0;
-    a.g_tile0[1] = a.n_tiles;
-    a.g_y[0] = y;
-    a.g_N[0] = w->N;
-    a.g_wscale[0] = w->w8_scale;
+    a.groups = count;
     mq::WMaps maps{};
-    maps.m[0] = w->tm_w8;
-    const int64_t tr = trace_begin(s, MQ_TRACE_GEMM_CACHED, w->type, M, w->N, w->K);
+    int nt = 0;
+    for (int g = 0; g < count; ++g) {
+        a.g_tile0[g] = nt;
+        a.g_y[g] = ys[g];
+        a.g_N[g] = ws[g]->N;
+        a.g_wscale[g] = ws[g]->w8_scale;
+        maps.m[g] = ws[g]->tm_w8;
+        nt += static_cast<int>((ws[g]->N + 127) / 128);
+    }
+    a.g_tile0[count] = nt;
+    a.n_tiles = nt;
+    const int64_t tr = trace_begin(s, MQ_TRACE_GEMM_CACHED, w->type, M, n_total, w->K);
     cudaError_t e = mq::launch_gemm_e4m3(maps, tm_x, a, plan, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "e4m3 GEMM launch");
@@ -962,6 +970,49 @@ int mq_gemm_e4m3(const void *x8, const float *x_scale, mq_handle w, float *y, in
     if (e != cudaSuccess)
         return cuda_fail(e, "split-K reduce launch");
     trace_mark(tr, 2, s, plan.split > 1 && plan.tiles > plan.full_tiles);
+    return MQ_OK;
+}
+
+}  // namespace
+
+int mq_gemm_e4m3(const void *x8, const float *x_scale, mq_handle w, float *y, int64_t M, void *stream)
+{
+    return mq_gemm_e4m3_grouped(x8, x_scale, &w, 1, &y, M, stream);
+}
+
+int mq_gemm_e4m3_grouped(const void *x8, const float *x_scale, const mq_handle *w, int count, float *const *y,
+                         int64_t M, void *stream)
+{
+    if (!w || !y)
+        return fail(MQ_ERR_INVALID, "%s is NULL", w ? "y" : "w");
+    if (!x_scale)
+        return fail(MQ_ERR_INVALID, "x_scale is NULL");
+    if (count < 1 || count > mq::kMaxGroup)
+        return fail(MQ_ERR_INVALID, "count=%d: need 1 <= count <= %d", count, mq::kMaxGroup);
+    bool one_launch = true;
+    for (int g = 0; g < count; ++g) {
+        int rc = check_gemm_args(x8, w[g], y[g], M);
+        if (rc)
+            return rc;
+        if (!w[g]->w8)
+            return fail(MQ_ERR_NO_CACHE, "member %d was registered without MQ_REG_E4M3: it has no e4m3 copy", g);
+        if (w[g]->K != w[0]->K)
+            return fail(MQ_ERR_SHAPE, "member %d has K=%lld, member 0 has K=%lld: a group shares X", g,
+                        (long long)w[g]->K, (long long)w[0]->K);
+        if (w[g]->device != w[0]->device)
+            return fail(MQ_ERR_INVALID, "member %d is registered on device %d, member 0 on %d", g, w[g]->device,
+                        w[0]->device);
+        if (w[g]->N % 128 != 0)
+            one_launch = false;
+    }
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (one_launch || count == 1)
+        return run_e4m3_group(x8, x_scale, w, y, count, M, s);
+    for (int g = 0; g < count; ++g) {
+        int rc = run_e4m3_group(x8, x_scale, &w[g], &y[g], 1, M, s);
+        if (rc)
+            return rc;
+    }
     return MQ_OK;
 }
 

@@ -3,7 +3,9 @@
     python -m quantized_weight_prefill_gguf_gb300.profile_case \
         --case fused --type q4_K --N 18944 --K 3584 --M 32 --reps 3
 
-Cases: cached (mq_gemm), fused (mq_gemm_fused), decode (mq_dequantize).
+Cases: cached (mq_gemm), fused (mq_gemm_fused), decode (mq_dequantize),
+e4m3 (mq_gemm_e4m3 on activations quantized once before), quant
+(mq_quantize_e4m3 of the M x K activations).
 Inputs are the seeded synthetic blocks of the given shape.  Prints the
 device time of each call from the library's trace events (not valid under a
 profiler, which serialises and replays kernels).
@@ -17,12 +19,12 @@ import torch
 import quantized_weight_prefill_gguf_gb300 as mq
 from quantized_weight_prefill_gguf_gb300 import synth
 
-TYPES = {"q4_K": synth.Q4_K, "q6_K": synth.Q6_K, "q8_0": synth.Q8_0}
+TYPES = {synth.TYPE_NAME[t]: t for t in synth.BLOCK}
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["cached", "fused", "decode"], required=True)
+    ap.add_argument("--case", choices=["cached", "fused", "decode", "e4m3", "quant"], required=True)
     ap.add_argument("--type", choices=sorted(TYPES), default="q4_K")
     ap.add_argument("--N", type=int, required=True)
     ap.add_argument("--K", type=int, required=True)
@@ -38,6 +40,17 @@ def main(argv=None):
     if args.case == "decode":
         out = torch.empty((args.N, args.K), dtype=torch.float16, device="cuda")
         fn = lambda: mq.mq_dequantize(qtype, q, args.N, args.K, out)  # noqa: E731
+    elif args.case in ("e4m3", "quant"):
+        h = mq.mq_register_weight(qtype, q, args.N, args.K, flags=mq.MQ_REG_E4M3)
+        x = torch.from_numpy(synth.activations(g, args.M, args.K)).cuda()
+        x8 = torch.empty((args.M, args.K), dtype=torch.uint8, device="cuda")
+        sx = torch.empty(args.M, dtype=torch.float32, device="cuda")
+        mq.mq_quantize_e4m3(x, x8, sx)
+        y = torch.empty((args.M, args.N), dtype=torch.float32, device="cuda")
+        if args.case == "quant":
+            fn = lambda: mq.mq_quantize_e4m3(x, x8, sx)  # noqa: E731
+        else:
+            fn = lambda: mq.mq_gemm_e4m3(x8, sx, h, y, args.M)  # noqa: E731
     else:
         flags = mq.MQ_REG_NO_CACHE if args.case == "fused" else 0
         h = mq.mq_register_weight(qtype, q, args.N, args.K, flags=flags)

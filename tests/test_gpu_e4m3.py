@@ -126,6 +126,34 @@ def test_gemm_matches_oracle(orc, qtype, N, K, M):
     assert rel < 0.1, f"quantization error {rel:.3f} vs the f16 path"
 
 
+@pytest.mark.parametrize("members,K,M", [
+    ([(synth.Q4_K, 384), (synth.Q4_K, 128), (synth.Q4_K, 128)], 512, 64),    # one launch
+    ([(synth.Q4_K, 1024), (synth.Q6_K, 512)], 768, 256),                     # split-K tail inside the group
+    ([(synth.Q4_K, 200), (synth.Q8_0, 128)], 512, 48),                       # N % 128 != 0: one after another
+])
+def test_grouped_matches_oracle(orc, members, K, M):
+    torch = torch_cuda()
+    mq = _mq()
+    g = synth.rng(K + M)
+    datas = [synth.weight_bytes(g, qt, N, K) for qt, N in members]
+    hs = [mq.mq_register_weight(qt, dev(d), N, K, flags=mq.MQ_REG_E4M3) for (qt, N), d in zip(members, datas)]
+    x = dev(synth.activations(g, M, K))
+    x8 = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    sx = torch.empty(M, dtype=torch.float32, device="cuda")
+    mq.mq_quantize_e4m3(x, x8, sx)
+    ys = [torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") for _, N in members]
+    mq.mq_gemm_e4m3_grouped(x8, sx, hs, ys, M)
+    mq.mq_stream_status()
+    X8, SX = x8.cpu().numpy(), sx.cpu().numpy()
+    for i, (h, y) in enumerate(zip(hs, ys)):
+        codes, scales = h.e4m3_tensors()
+        ref = orc.gemm_e4m3_f64(X8, SX, codes.cpu().numpy()[:, :K], scales.cpu().numpy())
+        assert_gemm_close(y.cpu().numpy(), ref, f"member {i}")
+        del codes, scales
+    for h in hs:
+        h.release()
+
+
 def test_layer_full_size_sampled(orc):
     """Every GEMM of the 7B layer at M = 2048 through the e4m3 path, ~1500
     sampled outputs each against the oracle; the relative distance to the
