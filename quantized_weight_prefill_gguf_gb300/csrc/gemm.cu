@@ -33,6 +33,13 @@
 // elements, and each of its four MMAs (kind::f8f6f4, K = 32) advances 32
 // bytes as for f16; the epilogue scales by the weight row's and the token's
 // quantization scales.
+//
+// CTA pairs (PAIR): two CTAs of a cluster take adjacent 128-row weight
+// tiles of the same token tile.  Each loads its own weight tile and half of
+// the token tile, multicast into both CTAs' shared memory, so a stage costs
+// an SM 16 + BN*64 bytes of L2 reads instead of 16 + 2*BN*64 KB.  A
+// stage's "empty" barrier then counts both CTAs' MMA commits: neither
+// producer refills a stage its peer may still be reading.
 #include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -56,8 +63,9 @@ template <int BN> struct Cfg {
 };
 
 // The kernel body: F8 selects e4m3 operands (K step kBK8, kind::f8f6f4,
-// scaled epilogue) over f16 (K step kBK, kind::f16).
-template <int BN, bool F8>
+// scaled epilogue) over f16 (K step kBK, kind::f16); PAIR runs the CTA as
+// one of a cluster pair (tm_x's box is then BN/2 tokens high).
+template <int BN, bool F8, bool PAIR>
 __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &tm_x, const GemmArgs &a)
 {
     using C = Cfg<BN>;
@@ -79,7 +87,7 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], PAIR ? 2 : 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
@@ -99,10 +107,14 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
         prefetch_tensormap(&tm_x);
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();   // the peer's barriers exist before any multicast reaches them
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     grid_dep_launch();
+    const UnitWalk wk = unit_walk(a);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -115,9 +127,10 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
             uint32_t issued = 0, issue_parity = 0;   // per-stage: load in flight, its phase parity
             bool ok = a.stall_producer == 0;
             int pre = 0;
-            for (int u = blockIdx.x; ok && pre < C::kStages && u < a.units; u += gridDim.x) {
-                const UnitInfo ui = unit_info(a, u);
-                const int nt = ui.tile / a.m_tiles;
+            for (int u = wk.first; ok && pre < C::kStages && u < a.units; u += wk.stride) {
+                const UnitInfo ui = unit_info(a, u, wk.rank);
+                int nt, mt;
+                tile_coords(a, ui.tile, nt, mt);
                 const int g = group_of(a, nt);
                 const int n0 = (nt - a.g_tile0[g]) * kTileRows;
                 for (int kb = ui.kb0; kb < ui.kb1 && pre < C::kStages; ++kb, ++pre) {
@@ -128,17 +141,24 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
             }
             grid_dep_wait();
             int step = 0;
-            for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
-                const UnitInfo ui = unit_info(a, u);
-                const int nt = ui.tile / a.m_tiles;
+            // the token rows this CTA loads: all BN, or its half of the pair's
+            const int b_off = PAIR ? wk.rank * (BN / 2) : 0;
+            uint8_t *sB_own = sB + b_off * 128;
+            for (int u = wk.first; ok && u < a.units; u += wk.stride) {
+                const UnitInfo ui = unit_info(a, u, wk.rank);
+                int nt, mt;
+                tile_coords(a, ui.tile, nt, mt);
                 const int g = group_of(a, nt);
                 const CUtensorMap *tmw = &tm_w.m[g];
                 const int n0 = (nt - a.g_tile0[g]) * kTileRows;   // row inside member g
-                const int m0 = (ui.tile % a.m_tiles) * BN;
+                const int m0 = mt * BN + b_off;
                 for (int kb = ui.kb0; kb < ui.kb1; ++kb, ++step) {
                     if (step < pre) {
                         // weight tile already requested (stage == step, phase 0)
-                        tma_load_2d(sB + stage * C::kBBytes, &tm_x, &full[stage], kb * kStep, m0);
+                        if constexpr (PAIR)
+                            tma_load_2d_mc(sB_own + stage * C::kBBytes, &tm_x, &full[stage], kb * kStep, m0, 0x3);
+                        else
+                            tma_load_2d(sB + stage * C::kBBytes, &tm_x, &full[stage], kb * kStep, m0);
                         if (++stage == C::kStages) {
                             stage = 0;
                             phase ^= 1u;
@@ -151,7 +171,10 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
                     }
                     mbar_arrive_expect_tx(&full[stage], kABytes + C::kBBytes);
                     tma_load_2d(sA + stage * kABytes, tmw, &full[stage], kb * kStep, n0);
-                    tma_load_2d(sB + stage * C::kBBytes, &tm_x, &full[stage], kb * kStep, m0);
+                    if constexpr (PAIR)
+                        tma_load_2d_mc(sB_own + stage * C::kBBytes, &tm_x, &full[stage], kb * kStep, m0, 0x3);
+                    else
+                        tma_load_2d(sB + stage * C::kBBytes, &tm_x, &full[stage], kb * kStep, m0);
                     issued |= 1u << stage;
                     issue_parity = (issue_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) {
@@ -183,8 +206,8 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
-                const UnitInfo ui = unit_info(a, u);
+            for (int u = wk.first; ok && u < a.units; u += wk.stride) {
+                const UnitInfo ui = unit_info(a, u, wk.rank);
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, a.status))
                     break;
                 tc_fence_after();
@@ -207,7 +230,10 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
                         else
                             umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > ui.kb0 || k > 0) ? 1u : 0u);
                     }
-                    umma_commit(&empty[stage]);
+                    if constexpr (PAIR)
+                        umma_commit_mc(&empty[stage], 0x3);   // frees the stage in both CTAs
+                    else
+                        umma_commit(&empty[stage]);
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -233,7 +259,10 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
     }
 
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();   // no CTA leaves while its peer may still write into it
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
@@ -244,14 +273,37 @@ template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_cached(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
 {
-    gemm_body<BN, false>(tm_w, tm_x, a);
+    gemm_body<BN, false, false>(tm_w, tm_x, a);
+}
+
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_gemm_cached_pair(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
+{
+    gemm_body<BN, false, true>(tm_w, tm_x, a);
 }
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_e4m3(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
 {
-    gemm_body<BN, true>(tm_w, tm_x, a);
+    gemm_body<BN, true, false>(tm_w, tm_x, a);
+}
+
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_gemm_e4m3_pair(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
+{
+    gemm_body<BN, true, true>(tm_w, tm_x, a);
+}
+
+template <int BN, bool F8, bool PAIR>
+constexpr auto gemm_kernel()
+{
+    if constexpr (PAIR)
+        return F8 ? k_gemm_e4m3_pair<BN> : k_gemm_cached_pair<BN>;
+    else
+        return F8 ? k_gemm_e4m3<BN> : k_gemm_cached<BN>;
 }
 
 // Fixed-order split-K reduction: Y = sum over p = 0..split-1 of the partial
@@ -271,10 +323,11 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(const GemmArgs a, int bn)
     if (e >= plane)
         return;
     const int col = e >> 7, row = e & 127;
-    const int nt = tile / a.m_tiles;
+    int nt, mt;
+    tile_coords(a, tile, nt, mt);
     const int g = group_of(a, nt);
     const int64_t Ng = a.g_N[g];
-    const int64_t m = static_cast<int64_t>(tile % a.m_tiles) * bn + col;
+    const int64_t m = static_cast<int64_t>(mt) * bn + col;
     const int64_t n = static_cast<int64_t>(nt - a.g_tile0[g]) * kTileRows + row;   // row inside member g
     if (m >= a.M || n >= Ng)
         return;
@@ -303,11 +356,11 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(const GemmArgs a, int bn)
     }
 }
 
-template <int BN, bool F8>
+template <int BN, bool F8, bool PAIR>
 cudaError_t launch_bn(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p, cudaStream_t s)
 {
     using C = Cfg<BN>;
-    auto *kern = F8 ? k_gemm_e4m3<BN> : k_gemm_cached<BN>;
+    auto *kern = gemm_kernel<BN, F8, PAIR>();
     static bool attr_done[64] = {};   // the attribute is set once per device (per instantiation)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -328,7 +381,7 @@ cudaError_t launch_bn(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a,
 }  // namespace
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available, int bn_override,
-                   int kstep)
+                   int kstep, int pair_clusters)
 {
     GemmPlan p{};
     // The fused path keeps a whole 256-element K chunk of activations per
@@ -347,44 +400,61 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t
     const int64_t n_tiles = (N + kTileRows - 1) / kTileRows;
     const int64_t kblocks = (K + kstep - 1) / kstep;
     const int64_t groups = (kblocks + p.kb_align - 1) / p.kb_align;
-    p.tiles = static_cast<int>(m_tiles * n_tiles);
+    // Work items: tiles on `slots` SMs, or pair tiles (two CTA tiles each,
+    // the second a phantom past N when the weight-row tiles are odd) on
+    // `slots` resident clusters.
+    p.pair = (!fused && pair_clusters > 0) ? 1 : 0;
+    const int per = p.pair ? 2 : 1;
+    const int slots = p.pair ? pair_clusters : sms;
+    const int items = static_cast<int>(m_tiles * (p.pair ? (n_tiles + 1) / 2 : n_tiles));
+    int full_items = items;
     p.split = 1;
-    p.full_tiles = p.tiles;
-    // Split-K tail: the tiles of the last, partial wave are split so that
+    // Split-K tail: the items of the last, partial wave are split so that
     // the wave fills the SMs; each part keeps at least 4 K steps.
-    const int tail = p.tiles % sms;
+    const int tail = items % slots;
     if (tail != 0) {
-        int s = sms / tail;
+        int s = slots / tail;
         const int64_t max_parts = fused ? groups : std::max<int64_t>(1, kblocks / 4);
         s = static_cast<int>(std::min<int64_t>(s, max_parts));
         s = std::min(s, kMaxSplit);
         if (s >= 2) {
-            const int64_t bytes = static_cast<int64_t>(tail) * s * p.bn * kTileRows * 4;
+            const int64_t bytes = static_cast<int64_t>(tail) * per * s * p.bn * kTileRows * 4;
             if (bytes <= ws_available) {
                 p.split = s;
-                p.full_tiles = p.tiles - tail;
+                full_items = items - tail;
                 p.ws_bytes = bytes;
             }
         }
     }
-    p.units = p.full_tiles + (p.tiles - p.full_tiles) * p.split;
-    p.grid = std::min(p.units, sms);
+    p.tiles = items * per;
+    p.full_tiles = full_items * per;
+    p.units = full_items + (items - full_items) * p.split;
+    p.grid = std::min(p.units, slots) * per;
     return p;
 }
 
-int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused, int bn_override, int kstep)
+int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused, int bn_override, int kstep,
+                             int pair_clusters)
 {
-    return plan_gemm(M, N, K, sms, fused, INT64_MAX, bn_override, kstep).ws_bytes;
+    return plan_gemm(M, N, K, sms, fused, INT64_MAX, bn_override, kstep, pair_clusters).ws_bytes;
 }
 
 cudaError_t launch_gemm_cached(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p,
                                cudaStream_t s)
 {
+    if (p.pair) {
+        switch (p.bn) {
+        case 256: return launch_bn<256, false, true>(tw, tx, a, p, s);
+        case 128: return launch_bn<128, false, true>(tw, tx, a, p, s);
+        case 64: return launch_bn<64, false, true>(tw, tx, a, p, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (p.bn) {
-    case 256: return launch_bn<256, false>(tw, tx, a, p, s);
-    case 128: return launch_bn<128, false>(tw, tx, a, p, s);
-    case 64: return launch_bn<64, false>(tw, tx, a, p, s);
-    case 32: return launch_bn<32, false>(tw, tx, a, p, s);
+    case 256: return launch_bn<256, false, false>(tw, tx, a, p, s);
+    case 128: return launch_bn<128, false, false>(tw, tx, a, p, s);
+    case 64: return launch_bn<64, false, false>(tw, tx, a, p, s);
+    case 32: return launch_bn<32, false, false>(tw, tx, a, p, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -392,12 +462,57 @@ cudaError_t launch_gemm_cached(const WMaps &tw, const CUtensorMap &tx, const Gem
 cudaError_t launch_gemm_e4m3(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p,
                              cudaStream_t s)
 {
+    if (p.pair) {
+        switch (p.bn) {
+        case 256: return launch_bn<256, true, true>(tw, tx, a, p, s);
+        case 128: return launch_bn<128, true, true>(tw, tx, a, p, s);
+        case 64: return launch_bn<64, true, true>(tw, tx, a, p, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (p.bn) {
-    case 256: return launch_bn<256, true>(tw, tx, a, p, s);
-    case 128: return launch_bn<128, true>(tw, tx, a, p, s);
-    case 64: return launch_bn<64, true>(tw, tx, a, p, s);
-    case 32: return launch_bn<32, true>(tw, tx, a, p, s);
+    case 256: return launch_bn<256, true, false>(tw, tx, a, p, s);
+    case 128: return launch_bn<128, true, false>(tw, tx, a, p, s);
+    case 64: return launch_bn<64, true, false>(tw, tx, a, p, s);
+    case 32: return launch_bn<32, true, false>(tw, tx, a, p, s);
     default: return cudaErrorInvalidValue;
+    }
+}
+
+// Clusters of two that can be resident at once, per device and kernel
+// (cached after the first query).
+template <int BN, bool F8>
+int pair_clusters_bn()
+{
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 0;
+    if (cached[dev] != 0)
+        return cached[dev] > 0 ? cached[dev] : 0;
+    using C = Cfg<BN>;
+    auto *kern = gemm_kernel<BN, F8, true>();
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) == cudaSuccess) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::kSmem;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
+            n = 0;
+    }
+    cudaGetLastError();
+    cached[dev] = n > 0 ? n : -1;
+    return n > 0 ? n : 0;
+}
+
+int pair_clusters_for(int bn, bool e4m3)
+{
+    switch (bn) {
+    case 256: return e4m3 ? pair_clusters_bn<256, true>() : pair_clusters_bn<256, false>();
+    case 128: return e4m3 ? pair_clusters_bn<128, true>() : pair_clusters_bn<128, false>();
+    case 64: return e4m3 ? pair_clusters_bn<64, true>() : pair_clusters_bn<64, false>();
+    default: return 0;
     }
 }
 

@@ -31,7 +31,9 @@ cudaError_t launch_dequant(int type, const void *q, int64_t nblocks, __half *out
 // A single weight is the group of one (g_y[0] = y, g_N[0] = N).
 constexpr int kMaxGroup = 4;
 
-// K elements per pipeline stage of the 8-bit (e4m3) GEMM: one 128-byte row.
+// K elements per pipeline stage of the GEMMs: one 128-byte swizzle row of
+// f16 (64) or of 8-bit e4m3 (128) operands.
+constexpr int kKStepF16 = 64;
 constexpr int kKStepE4m3 = 128;
 
 struct GemmArgs {
@@ -55,6 +57,7 @@ struct GemmArgs {
     int64_t raw_rb;      // fused path: bytes per weight row (when rows start on block boundaries)
     int stall_producer;  // failure-injection hook: the weight producer issues nothing, so the
                          // consumers' bounded waits run out (tests of the timeout path)
+    int pair;                       // CTAs run in clusters of two (see tile_coords)
     const float *x_scale;           // 8-bit path: per-token scale of X [M]
     const float *g_wscale[kMaxGroup];  // 8-bit path: per-row scale of each member's weight
     int groups;                     // members of the group (1 for a single weight)
@@ -90,6 +93,7 @@ struct RawMaps {
 
 struct GemmPlan {
     int bn;              // tokens per tile (MMA N)
+    int pair;            // 1: CTAs in clusters of two sharing the token tile
     int kb_align;        // split boundaries in K steps (4 for the fused path)
     int split;
     int full_tiles;
@@ -102,12 +106,19 @@ struct GemmPlan {
 // Choose tile width, split-K and grid for an M x N x K problem on `sms` SMs.
 // bn_override > 0 forces the cached path's tile width (32, 64, 128 or 256).
 // kstep: K elements per pipeline stage (64 for f16 operands, 128 for 8-bit).
+// pair_clusters > 0: plan for CTA pairs (clusters of two sharing the token
+// tile), at most pair_clusters of them resident; tiles, units and grid then
+// count pair-major tiles, pair units and CTAs.
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t ws_available,
-                   int bn_override = 0, int kstep = 64);
+                   int bn_override = 0, int kstep = 64, int pair_clusters = 0);
 
 // Workspace bytes the plan would use with an unlimited workspace.
 int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused, int bn_override = 0,
-                             int kstep = 64);
+                             int kstep = 64, int pair_clusters = 0);
+
+// Clusters of two cached-GEMM CTAs (tile width bn, f16 or e4m3 operands)
+// that can be resident at once on the current device (0 if none).
+int pair_clusters_for(int bn, bool e4m3);
 
 // Cached path: tm_w.m[g] maps member g's f16 cache [N_g, ldk_g] (box 64 x
 // 128), tm_x maps X [M, K] (box 64 x bn).  All 128-byte swizzled.

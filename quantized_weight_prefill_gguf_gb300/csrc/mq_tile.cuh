@@ -10,7 +10,7 @@
 
 namespace mq {
 
-constexpr int kBK = 64;                       // K elements per MMA stage (one 128-byte swizzle row of f16)
+constexpr int kBK = kKStepF16;                // K elements per MMA stage (one 128-byte swizzle row of f16)
 constexpr int kBK8 = kKStepE4m3;              // the same 128-byte row of 8-bit operands
 constexpr int kTileRows = 128;                // weight rows per tile (the MMA's M)
 constexpr int kABytes = kTileRows * kBK * 2;  // 16 KB f16 weight tile per stage
@@ -19,31 +19,63 @@ struct UnitInfo {
     int tile, kb0, kb1, part, slot;
 };
 
+// Weight-row tile nt and token tile mt of tile t.  Single CTAs: t = nt *
+// m_tiles + mt.  CTA pairs (a.pair): pair-major numbering, t = 2p + r for
+// pair tile p = (nt / 2) * m_tiles + mt and r = nt % 2, so the two CTAs of a
+// cluster take tiles 2p and 2p+1 -- adjacent weight rows, the same tokens.
+__host__ __device__ inline void tile_coords(const GemmArgs &a, int t, int &nt, int &mt)
+{
+    if (a.pair) {
+        const int p = t >> 1;
+        nt = 2 * (p / a.m_tiles) + (t & 1);
+        mt = p % a.m_tiles;
+    } else {
+        nt = t / a.m_tiles;
+        mt = t % a.m_tiles;
+    }
+}
+
 // Unit u of the schedule: tiles [0, full_tiles) take all of K; after them,
 // each remaining tile is `split` consecutive units over K-ranges whose
-// boundaries are multiples of kb_align K steps.  Tile t covers weight rows
-// (t / m_tiles)*128 .. +127 and tokens (t % m_tiles)*BN .. +BN-1.
-__device__ __forceinline__ UnitInfo unit_info(const GemmArgs &a, int u)
+// boundaries are multiples of kb_align K steps (tile_coords places a tile).
+// With CTA pairs, u counts pair units and rank r (0 or 1) picks the pair's
+// tile: the two CTAs of a cluster run the same K-ranges in step.
+__device__ __forceinline__ UnitInfo unit_info(const GemmArgs &a, int u, int r = 0)
 {
-    UnitInfo r;
-    if (u < a.full_tiles) {
-        r.tile = u;
-        r.kb0 = 0;
-        r.kb1 = a.kblocks;
-        r.part = -1;
-        r.slot = 0;
+    UnitInfo ui;
+    const int full = a.pair ? a.full_tiles >> 1 : a.full_tiles;
+    if (u < full) {
+        ui.tile = a.pair ? 2 * u + r : u;
+        ui.kb0 = 0;
+        ui.kb1 = a.kblocks;
+        ui.part = -1;
+        ui.slot = 0;
     } else {
-        const int v = u - a.full_tiles;
-        r.slot = v / a.split;
-        r.part = v - r.slot * a.split;
-        r.tile = a.full_tiles + r.slot;
+        const int v = u - full;
+        const int s = v / a.split;
+        ui.part = v - s * a.split;
+        ui.slot = a.pair ? 2 * s + r : s;
+        ui.tile = a.full_tiles + ui.slot;
         const int groups = (a.kblocks + a.kb_align - 1) / a.kb_align;
-        const int g0 = static_cast<int>(static_cast<int64_t>(r.part) * groups / a.split);
-        const int g1 = static_cast<int>(static_cast<int64_t>(r.part + 1) * groups / a.split);
-        r.kb0 = g0 * a.kb_align;
-        r.kb1 = g1 * a.kb_align < a.kblocks ? g1 * a.kb_align : a.kblocks;
+        const int g0 = static_cast<int>(static_cast<int64_t>(ui.part) * groups / a.split);
+        const int g1 = static_cast<int>(static_cast<int64_t>(ui.part + 1) * groups / a.split);
+        ui.kb0 = g0 * a.kb_align;
+        ui.kb1 = g1 * a.kb_align < a.kblocks ? g1 * a.kb_align : a.kblocks;
     }
-    return r;
+    return ui;
+}
+
+// This CTA's walk over the units: first unit, stride, and pair rank.
+struct UnitWalk {
+    int first, stride, rank;
+};
+
+__device__ __forceinline__ UnitWalk unit_walk(const GemmArgs &a)
+{
+    if (a.pair)
+        return UnitWalk{static_cast<int>(blockIdx.x >> 1), static_cast<int>(gridDim.x >> 1),
+                        static_cast<int>(blockIdx.x & 1)};
+    return UnitWalk{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), 0};
 }
 
 // Epilogue role, run by four warps whose (warp index % 4) are 0..3: warp w
@@ -72,17 +104,19 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
     const int row = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-        const UnitInfo ui = unit_info(a, u);
+    const UnitWalk wk = unit_walk(a);
+    for (int u = wk.first; u < a.units; u += wk.stride) {
+        const UnitInfo ui = unit_info(a, u, wk.rank);
         const bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, a.status);
         if (!__all_sync(0xFFFFFFFFu, ok))
             break;
         tc_fence_after();
-        const int nt = ui.tile / a.m_tiles;
+        int nt, mt;
+        tile_coords(a, ui.tile, nt, mt);
         const int g = group_of(a, nt);
         const int64_t Ng = a.g_N[g];
         const int64_t n = static_cast<int64_t>(nt - a.g_tile0[g]) * kTileRows + row;   // row inside member g
-        const int64_t m0 = static_cast<int64_t>(ui.tile % a.m_tiles) * BN;
+        const int64_t m0 = static_cast<int64_t>(mt) * BN;
         const bool two = NPART == 2 && ui.kb1 - ui.kb0 > kb_split;
         float wscale = 0.0f;
         if constexpr (SCALED)
