@@ -296,6 +296,26 @@ int mq_gemm_e4m3_grouped(const void *x8, const float *x_scale, const mq_handle *
 int mq_weight_e4m3_info(mq_handle w, int64_t *ldk8, const void **codes, const float **scales);
 
 /*
+ * mq_debug_schedule -- the work plan of one GEMM launch, for tests and
+ * tuning; host only, launches nothing, needs no device.
+ *  M, N, K, sms   the problem and the SM count to plan for.
+ *  path           0 cached f16, 1 fused, 2 e4m3.
+ *  pair_clusters  > 0: plan CTA pairs with this many resident clusters
+ *                 (ignored for the fused path); 0: single CTAs.
+ *  plan_out       9 values: tile width, pair flag, split, full tiles,
+ *                 tiles, units, grid, split-K workspace bytes, split
+ *                 alignment in K steps.
+ *  units          receives up to cap units, 8 int32 each: CTA, tile,
+ *                 weight-row tile, token tile, first and end K step, split
+ *                 part (-1: whole K), workspace slot.
+ *  count          the number of units the CTAs run (may exceed cap).
+ * The kernels' own schedule code computes it.  Errors: MQ_ERR_INVALID.
+ */
+int mq_debug_schedule(int64_t M, int64_t N, int64_t K, int sms, int path, int pair_clusters, int64_t *plan_out,
+                      int32_t *units, int64_t cap, int64_t *count);
+
+/*
+ * mq_gemm_noalloc -- the cached GEMM/*
  * mq_gemm_noalloc -- the cached GEMM (same result as mq_gemm, same
  * arguments) for callers that cannot allocate device memory: code that runs
  * while a stream is captured into a CUDA graph in global capture mode (where

@@ -29,7 +29,7 @@ EXPORTS = ("mq_register_weight", "mq_release_weight", "mq_weight_info", "mq_dequ
            "mq_stream_status", "mq_launch_count", "mq_error_string", "mq_last_error_detail", "mq_version",
            "mq_trace_enable", "mq_trace_count", "mq_trace_read", "mq_gemm_noalloc", "mq_gemm_grouped",
            "mq_gemm_scratch", "mq_quantize_e4m3", "mq_gemm_e4m3", "mq_weight_e4m3_info",
-           "mq_gemm_e4m3_grouped")
+           "mq_gemm_e4m3_grouped", "mq_debug_schedule")
 MQ_TRACE_GEMM_CACHED, MQ_TRACE_GEMM_FUSED, MQ_TRACE_DECODE = 1, 2, 3
 
 
@@ -63,6 +63,8 @@ def _load() -> ctypes.CDLL:
                                  ctypes.c_int),
         "mq_weight_e4m3_info": ([_P, ctypes.POINTER(_I64), ctypes.POINTER(_P), ctypes.POINTER(_P)], ctypes.c_int),
         "mq_gemm_grouped": ([_P, ctypes.POINTER(_P), ctypes.c_int, ctypes.POINTER(_P), _I64, _P], ctypes.c_int),
+        "mq_debug_schedule": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _I64, _P],
+                              ctypes.c_int),
         "mq_get_m_gate": ([], _I64),
         "mq_set_m_gate": ([_I64], ctypes.c_int),
         "mq_reserve_workspace": ([_I64], ctypes.c_int),
@@ -260,6 +262,21 @@ def mq_gemm_e4m3_grouped(x8, x_scale, ws, ys, M: int | None = None, stream=None)
     yarr = (_P * n)(*[_ptr(y) for y in ys])
     _check(_lib().mq_gemm_e4m3_grouped(_ptr(x8), _ptr(x_scale), harr, n, yarr, M if M is not None else x8.shape[0],
                                        _stream(stream)), "mq_gemm_e4m3_grouped")
+
+
+def mq_debug_schedule(M: int, N: int, K: int, sms: int, path: int = 0, pair_clusters: int = 0):
+    """(plan dict, units [n, 8] int32 array) of a GEMM launch as the kernels
+    would run it (path 0 cached, 1 fused, 2 e4m3); host only."""
+    import numpy as np
+    plan = np.zeros(9, dtype=np.int64)
+    count = ctypes.c_int64()
+    _check(_lib().mq_debug_schedule(M, N, K, sms, path, pair_clusters, plan.ctypes.data, None, 0,
+                                    ctypes.byref(count)), "mq_debug_schedule")
+    units = np.zeros((max(count.value, 1), 8), dtype=np.int32)
+    _check(_lib().mq_debug_schedule(M, N, K, sms, path, pair_clusters, plan.ctypes.data, units.ctypes.data,
+                                    count.value, ctypes.byref(count)), "mq_debug_schedule")
+    keys = ("bn", "pair", "split", "full_tiles", "tiles", "units", "grid", "ws_bytes", "kb_align")
+    return dict(zip(keys, plan.tolist())), units[: count.value]
 
 
 def mq_get_m_gate() -> int:

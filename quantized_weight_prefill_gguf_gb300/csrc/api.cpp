@@ -877,6 +877,28 @@ int mq_gemm_scratch(const void *x, mq_handle w, float *y, int64_t M, void *scrat
     return run_gemm(x, &tmp, y, M, s, false);
 }
 
+int mq_debug_schedule(int64_t M, int64_t N, int64_t K, int sms, int path, int pair_clusters, int64_t *plan_out,
+                      int32_t *units, int64_t cap, int64_t *count)
+{
+    if (M < 1 || N < 1 || K < 1 || sms < 1 || path < 0 || path > 2 || pair_clusters < 0 || !plan_out || !count ||
+        (cap > 0 && !units))
+        return fail(MQ_ERR_INVALID, "mq_debug_schedule: bad argument");
+    const bool fused = path == 1;
+    const int kstep = path == 2 ? mq::kKStepE4m3 : mq::kKStepF16;
+    const mq::GemmPlan p = mq::plan_gemm(M, N, K, sms, fused, INT64_MAX, 0, kstep, fused ? 0 : pair_clusters);
+    plan_out[0] = p.bn;
+    plan_out[1] = p.pair;
+    plan_out[2] = p.split;
+    plan_out[3] = p.full_tiles;
+    plan_out[4] = p.tiles;
+    plan_out[5] = p.units;
+    plan_out[6] = p.grid;
+    plan_out[7] = p.ws_bytes;
+    plan_out[8] = p.kb_align;
+    *count = mq::schedule_units(p, M, N, K, kstep, units, cap);
+    return MQ_OK;
+}
+
 int mq_weight_e4m3_info(mq_handle w, int64_t *ldk8, const void **codes, const float **scales)
 {
     int rc = check_handle(w);

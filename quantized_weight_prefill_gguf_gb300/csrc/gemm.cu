@@ -433,6 +433,42 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t
     return p;
 }
 
+int64_t schedule_units(const GemmPlan &p, int64_t M, int64_t N, int64_t K, int kstep, int32_t *out, int64_t cap)
+{
+    GemmArgs a{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.m_tiles = static_cast<int>((M + p.bn - 1) / p.bn);
+    a.kblocks = static_cast<int>((K + kstep - 1) / kstep);
+    a.full_tiles = p.full_tiles;
+    a.split = p.split;
+    a.units = p.units;
+    a.kb_align = p.kb_align;
+    a.pair = p.pair;
+    int64_t n = 0;
+    for (int cta = 0; cta < p.grid; ++cta) {
+        const UnitWalk wk = unit_walk_of(a, cta, p.grid);
+        for (int u = wk.first; u < a.units; u += wk.stride, ++n) {
+            if (n >= cap)
+                continue;
+            const UnitInfo ui = unit_info(a, u, wk.rank);
+            int nt, mt;
+            tile_coords(a, ui.tile, nt, mt);
+            int32_t *r = out + 8 * n;
+            r[0] = cta;
+            r[1] = ui.tile;
+            r[2] = nt;
+            r[3] = mt;
+            r[4] = ui.kb0;
+            r[5] = ui.kb1;
+            r[6] = ui.part;
+            r[7] = ui.slot;
+        }
+    }
+    return n;
+}
+
 int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused, int bn_override, int kstep,
                              int pair_clusters)
 {

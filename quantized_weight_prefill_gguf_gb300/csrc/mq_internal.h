@@ -116,6 +116,11 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, bool fused, int64_t
 int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fused, int bn_override = 0,
                              int kstep = 64, int pair_clusters = 0);
 
+// The units every CTA of a planned launch runs, computed with the kernels'
+// own schedule code: 8 ints per unit (cta, tile, nt, mt, kb0, kb1, part,
+// slot), at most cap units written; returns the number of units.
+int64_t schedule_units(const GemmPlan &p, int64_t M, int64_t N, int64_t K, int kstep, int32_t *out, int64_t cap);
+
 // Clusters of two cached-GEMM CTAs (tile width bn, f16 or e4m3 operands)
 // that can be resident at once on the current device (0 if none).
 int pair_clusters_for(int bn, bool e4m3);

@@ -40,7 +40,7 @@ __host__ __device__ inline void tile_coords(const GemmArgs &a, int t, int &nt, i
 // boundaries are multiples of kb_align K steps (tile_coords places a tile).
 // With CTA pairs, u counts pair units and rank r (0 or 1) picks the pair's
 // tile: the two CTAs of a cluster run the same K-ranges in step.
-__device__ __forceinline__ UnitInfo unit_info(const GemmArgs &a, int u, int r = 0)
+__host__ __device__ inline UnitInfo unit_info(const GemmArgs &a, int u, int r = 0)
 {
     UnitInfo ui;
     const int full = a.pair ? a.full_tiles >> 1 : a.full_tiles;
@@ -70,12 +70,16 @@ struct UnitWalk {
     int first, stride, rank;
 };
 
-__device__ __forceinline__ UnitWalk unit_walk(const GemmArgs &a)
+__host__ __device__ inline UnitWalk unit_walk_of(const GemmArgs &a, int cta, int grid)
 {
     if (a.pair)
-        return UnitWalk{static_cast<int>(blockIdx.x >> 1), static_cast<int>(gridDim.x >> 1),
-                        static_cast<int>(blockIdx.x & 1)};
-    return UnitWalk{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), 0};
+        return UnitWalk{cta >> 1, grid >> 1, cta & 1};
+    return UnitWalk{cta, grid, 0};
+}
+
+__device__ __forceinline__ UnitWalk unit_walk(const GemmArgs &a)
+{
+    return unit_walk_of(a, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
 }
 
 // Epilogue role, run by four warps whose (warp index % 4) are 0..3: warp w
