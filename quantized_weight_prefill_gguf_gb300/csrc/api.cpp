@@ -248,17 +248,27 @@ int64_t current_gate()
     return env_int("MQ_M_GATE", 256);
 }
 
+// Whether 256-token tiles run as 2-SM MMAs (tcgen05.mma.cta_group::2,
+// the default; MQ_2SM=0 keeps multicast CTA pairs).
+bool two_sm_wanted() { return env_int("MQ_2SM", 1) != 0; }
+
 // Clusters of two to plan the cached or e4m3 GEMM with (0: single CTAs).
-// CTA pairs share each token tile between two weight-row tiles (measured on
-// the 7B layer at M = 2048: gate 178 -> 175 us f16, 100 -> 98 us e4m3, the
-// step ~1 % faster).  On unless MQ_PAIR=0, for tiles at least 64 tokens
-// wide, and only when the device can hold clusters of two of the kernel.
+// CTA pairs (on unless MQ_PAIR=0, for tiles at least 64 tokens wide, when
+// the device can hold clusters of two of the kernel) take adjacent weight-row
+// tiles of one token tile: at 256 tokens as one 2-SM MMA tile, narrower as
+// two CTAs sharing the token tile by multicast.
 int pair_clusters(int64_t M, int64_t N, int64_t K, int sms, int bn_override, int kstep, bool e4m3)
 {
     if (env_int("MQ_PAIR", 1) == 0)
         return 0;
     const mq::GemmPlan p0 = mq::plan_gemm(M, N, K, sms, false, 0, bn_override, kstep);
-    return p0.bn >= 64 ? mq::pair_clusters_for(p0.bn, e4m3) : 0;
+    return p0.bn >= 64 ? mq::pair_clusters_for(p0.bn, e4m3, p0.bn == 256 && two_sm_wanted()) : 0;
+}
+
+// 2-SM MMAs for a CTA-pair plan with 256-token tiles.
+int two_sm_on(const mq::GemmPlan &p)
+{
+    return (p.pair && p.bn == 256 && two_sm_wanted()) ? 1 : 0;
 }
 
 // Plan, workspace and launch of one GEMM: one weight (cached or fused), or a
@@ -296,8 +306,9 @@ int run_gemm_group(const void *x, const mq_handle *ws, float *const *ys, int cou
                 return rc;
         }
     }
-    const mq::GemmPlan plan =
+    mq::GemmPlan plan =
         mq::plan_gemm(M, n_total, w->K, d->sms, fused, splitk_on ? d->ws_bytes : 0, bn_override, mq::kKStepF16, pc);
+    plan.two_sm = two_sm_on(plan);
 
     CUtensorMap tm_x;
     CUresult cr = mq::encode_f16_2d(&tm_x, x, M, w->K, w->K, 64, plan.pair ? plan.bn / 2 : plan.bn);
@@ -965,8 +976,9 @@ int run_e4m3_group(const void *x8, const float *x_scale, const mq_handle *ws, fl
                 return rc;
         }
     }
-    const mq::GemmPlan plan =
+    mq::GemmPlan plan =
         mq::plan_gemm(M, n_total, w->K, d->sms, false, splitk_on ? d->ws_bytes : 0, 0, mq::kKStepE4m3, pc);
+    plan.two_sm = two_sm_on(plan);
     CUtensorMap tm_x;
     CUresult cr = mq::encode_u8_2d(&tm_x, x8, M, w->K, w->K, 128, plan.pair ? plan.bn / 2 : plan.bn);
     if (cr != CUDA_SUCCESS)

@@ -269,6 +269,223 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
     }
 }
 
+// ---------------------------------------------------------------- 2-SM MMAs
+// A CTA pair computes a 256 x BN tile with tcgen05.mma.cta_group::2: each
+// CTA stages its own 128 weight rows and half of the BN tokens (32 KB per
+// stage at BN = 256 instead of 48 KB), so shared memory holds seven stages
+// instead of four and each byte in flight covers half again as much MMA
+// time (the single-CTA kernel's loads could not hide the L2 latency: its
+// tensor pipe idled 30 % of the time; the 7B gate GEMM goes 174 -> 163 us).  The
+// even CTA issues the MMAs; each D half lands in its own CTA's TMEM.
+// Barriers: each CTA's TMA completes its own `full`; the odd CTA relays that
+// to the even CTA's `peer_full`; the MMA commits arrive on `empty` and
+// `tfull` of both CTAs; both CTAs' epilogues release the accumulator on the
+// even CTA's `tempty`.
+constexpr int kTwoSmAccs = 2;   // accumulators in TMEM (kTwoSmAccs * BN columns)
+
+template <int BN> struct Cfg2 {
+    static constexpr int kHalfB = (BN / 2) * 128;   // this CTA's half of a token stage
+    static constexpr int kStages = 7;   // 5 / 6 / 7 measured 166.5 / 164.8 / 163.3 us on the gate
+    static constexpr int kTmemCols = kTwoSmAccs * BN;
+    static constexpr int kSmem = 1024 + kStages * (kABytes + kHalfB) + 512;
+};
+
+template <int BN, bool F8>
+__device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorMap &tm_x, const GemmArgs &a)
+{
+    using C = Cfg2<BN>;
+    constexpr int kStep = F8 ? kBK8 : kBK;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sA = base;
+    uint8_t *sB = base + C::kStages * kABytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kHalfB);
+    uint64_t *peer_full = full + C::kStages;
+    uint64_t *empty = peer_full + C::kStages;
+    uint64_t *tfull = empty + C::kStages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&peer_full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 8);   // four epilogue warps in each CTA
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, C::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int g = 0; g < a.groups; ++g)
+            prefetch_tensormap(&tm_w.m[g]);
+        prefetch_tensormap(&tm_x);
+    }
+    tc_fence_before();
+    cluster_sync();   // barriers and TMEM of both CTAs exist before either uses the other's
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    grid_dep_launch();
+    const UnitWalk wk = unit_walk(a);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer: own weight rows, own half of the tokens
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, issue_parity = 0;
+            bool ok = a.stall_producer == 0;
+            int pre = 0;
+            for (int u = wk.first; ok && pre < C::kStages && u < a.units; u += wk.stride) {
+                const UnitInfo ui = unit_info(a, u, wk.rank);
+                int nt, mt;
+                tile_coords(a, ui.tile, nt, mt);
+                const int g = group_of(a, nt);
+                const int n0 = (nt - a.g_tile0[g]) * kTileRows;
+                for (int kb = ui.kb0; kb < ui.kb1 && pre < C::kStages; ++kb, ++pre) {
+                    mbar_arrive_expect_tx(&full[pre], kABytes + C::kHalfB);
+                    tma_load_2d(sA + pre * kABytes, &tm_w.m[g], &full[pre], kb * kStep, n0);
+                    issued |= 1u << pre;
+                }
+            }
+            grid_dep_wait();
+            int step = 0;
+            for (int u = wk.first; ok && u < a.units; u += wk.stride) {
+                const UnitInfo ui = unit_info(a, u, wk.rank);
+                int nt, mt;
+                tile_coords(a, ui.tile, nt, mt);
+                const int g = group_of(a, nt);
+                const CUtensorMap *tmw = &tm_w.m[g];
+                const int n0 = (nt - a.g_tile0[g]) * kTileRows;
+                const int m0 = mt * BN + static_cast<int>(rank) * (BN / 2);
+                for (int kb = ui.kb0; kb < ui.kb1; ++kb, ++step) {
+                    if (step < pre) {
+                        tma_load_2d(sB + stage * C::kHalfB, &tm_x, &full[stage], kb * kStep, m0);
+                        if (++stage == C::kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], kABytes + C::kHalfB);
+                    tma_load_2d(sA + stage * kABytes, tmw, &full[stage], kb * kStep, n0);
+                    tma_load_2d(sB + stage * C::kHalfB, &tm_x, &full[stage], kb * kStep, m0);
+                    issued |= 1u << stage;
+                    issue_parity = (issue_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                volatile int no_abort = 0;
+                for (int s = 0; s < C::kStages; ++s)
+                    if (issued & (1u << s))
+                        mbar_wait_bounded(&full[s], (issue_parity >> s) & 1u, &no_abort, a.status);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 1) {
+            // ---------------- relay: this CTA's stage landed -> the even CTA's peer_full
+            const uint32_t peer_full0 = mapa_shared(&peer_full[0], 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = wk.first; ok && u < a.units; u += wk.stride) {
+                const UnitInfo ui = unit_info(a, u, wk.rank);
+                for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cluster(peer_full0 + static_cast<uint32_t>(stage) * 8u);
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        } else if (lane == 0) {
+            // ---------------- MMA issuer (even CTA): M = 256 across the pair
+            constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(2 * kTileRows, BN) : idesc_f16_f32(2 * kTileRows, BN);
+            const uint64_t a_desc0 = sdesc_k_sw128(smem_u32(sA));
+            const uint64_t b_desc0 = sdesc_k_sw128(smem_u32(sB));
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int u = wk.first; ok && u < a.units; u += wk.stride) {
+                const UnitInfo ui = unit_info(a, u, wk.rank);
+                if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, a.status))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+                for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, a.status) ||
+                        !mbar_wait_bounded(&peer_full[stage], phase, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * kABytes) >> 4);
+                    const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * C::kHalfB) >> 4);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if constexpr (F8)
+                            umma_e4m3_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > ui.kb0 || k > 0) ? 1u : 0u);
+                        else
+                            umma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > ui.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit_pair_mc(&empty[stage], 0x3);
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                umma_commit_pair_mc(&tfull[acc], 0x3);
+                if (++acc == kTwoSmAccs) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            umma_commit_pair_mc(drain, 0x1);
+            volatile int no_abort = 0;
+            mbar_wait_bounded(drain, 0, &no_abort, a.status);
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5, this CTA's 128 rows of D
+        epilogue_role<BN, kTwoSmAccs, 1, F8>(a, tmem, tfull, tempty, abort_flag, warp, lane, 1, 0);
+    }
+
+    tc_fence_before();
+    cluster_sync();   // no CTA leaves (or frees TMEM) while its peer may still reach into it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, C::kTmemCols);
+    }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_cached(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
@@ -295,6 +512,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_gemm_e4m3_pair(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
 {
     gemm_body<BN, true, true>(tm_w, tm_x, a);
+}
+
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_gemm_cached_2sm(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
+{
+    gemm_body_2sm<BN, false>(tm_w, tm_x, a);
+}
+
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_gemm_e4m3_2sm(const __grid_constant__ WMaps tm_w, const __grid_constant__ CUtensorMap tm_x, const GemmArgs a)
+{
+    gemm_body_2sm<BN, true>(tm_w, tm_x, a);
+}
+
+template <bool F8>
+cudaError_t launch_2sm(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p, cudaStream_t s)
+{
+    using C = Cfg2<256>;
+    auto *kern = F8 ? k_gemm_e4m3_2sm<256> : k_gemm_cached_2sm<256>;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        if (e != cudaSuccess)
+            return e;
+        if (dev >= 0 && dev < 64)
+            attr_done[dev] = true;
+    }
+    e = launch_kernel(kern, dim3(p.grid), dim3(kThreads), C::kSmem, s, tw, tx, a);
+    note_launch();
+    return e;
 }
 
 template <int BN, bool F8, bool PAIR>
@@ -478,6 +731,8 @@ int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fuse
 cudaError_t launch_gemm_cached(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p,
                                cudaStream_t s)
 {
+    if (p.two_sm && p.pair && p.bn == 256)
+        return launch_2sm<false>(tw, tx, a, p, s);
     if (p.pair) {
         switch (p.bn) {
         case 256: return launch_bn<256, false, true>(tw, tx, a, p, s);
@@ -498,6 +753,8 @@ cudaError_t launch_gemm_cached(const WMaps &tw, const CUtensorMap &tx, const Gem
 cudaError_t launch_gemm_e4m3(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p,
                              cudaStream_t s)
 {
+    if (p.two_sm && p.pair && p.bn == 256)
+        return launch_2sm<true>(tw, tx, a, p, s);
     if (p.pair) {
         switch (p.bn) {
         case 256: return launch_bn<256, true, true>(tw, tx, a, p, s);
@@ -517,7 +774,7 @@ cudaError_t launch_gemm_e4m3(const WMaps &tw, const CUtensorMap &tx, const GemmA
 
 // Clusters of two that can be resident at once, per device and kernel
 // (cached after the first query).
-template <int BN, bool F8>
+template <int BN, bool F8, bool TWO_SM>
 int pair_clusters_bn()
 {
     static int cached[64] = {};
@@ -526,14 +783,14 @@ int pair_clusters_bn()
         return 0;
     if (cached[dev] != 0)
         return cached[dev] > 0 ? cached[dev] : 0;
-    using C = Cfg<BN>;
-    auto *kern = gemm_kernel<BN, F8, true>();
+    const int smem = TWO_SM ? Cfg2<BN>::kSmem : Cfg<BN>::kSmem;
+    auto *kern = TWO_SM ? (F8 ? k_gemm_e4m3_2sm<BN> : k_gemm_cached_2sm<BN>) : gemm_kernel<BN, F8, true>();
     int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) == cudaSuccess) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(2);
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = C::kSmem;
+        cfg.dynamicSmemBytes = smem;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
             n = 0;
     }
@@ -542,12 +799,15 @@ int pair_clusters_bn()
     return n > 0 ? n : 0;
 }
 
-int pair_clusters_for(int bn, bool e4m3)
+int pair_clusters_for(int bn, bool e4m3, bool two_sm)
 {
     switch (bn) {
-    case 256: return e4m3 ? pair_clusters_bn<256, true>() : pair_clusters_bn<256, false>();
-    case 128: return e4m3 ? pair_clusters_bn<128, true>() : pair_clusters_bn<128, false>();
-    case 64: return e4m3 ? pair_clusters_bn<64, true>() : pair_clusters_bn<64, false>();
+    case 256:
+        if (two_sm)
+            return e4m3 ? pair_clusters_bn<256, true, true>() : pair_clusters_bn<256, false, true>();
+        return e4m3 ? pair_clusters_bn<256, true, false>() : pair_clusters_bn<256, false, false>();
+    case 128: return e4m3 ? pair_clusters_bn<128, true, false>() : pair_clusters_bn<128, false, false>();
+    case 64: return e4m3 ? pair_clusters_bn<64, true, false>() : pair_clusters_bn<64, false, false>();
     default: return 0;
     }
 }

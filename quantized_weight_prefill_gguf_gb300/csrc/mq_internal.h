@@ -94,6 +94,7 @@ struct RawMaps {
 struct GemmPlan {
     int bn;              // tokens per tile (MMA N)
     int pair;            // 1: CTAs in clusters of two sharing the token tile
+    int two_sm;          // with pair and bn = 256: 2-SM MMAs (M = 256 across the pair)
     int kb_align;        // split boundaries in K steps (4 for the fused path)
     int split;
     int full_tiles;
@@ -121,9 +122,10 @@ int64_t plan_ws_bytes_wanted(int64_t M, int64_t N, int64_t K, int sms, bool fuse
 // slot), at most cap units written; returns the number of units.
 int64_t schedule_units(const GemmPlan &p, int64_t M, int64_t N, int64_t K, int kstep, int32_t *out, int64_t cap);
 
-// Clusters of two cached-GEMM CTAs (tile width bn, f16 or e4m3 operands)
-// that can be resident at once on the current device (0 if none).
-int pair_clusters_for(int bn, bool e4m3);
+// Clusters of two cached-GEMM CTAs (tile width bn, f16 or e4m3 operands,
+// multicast pairs or 2-SM MMAs) that can be resident at once on the current
+// device (0 if none).
+int pair_clusters_for(int bn, bool e4m3, bool two_sm);
 
 // Cached path: tm_w.m[g] maps member g's f16 cache [N_g, ldk_g] (box 64 x
 // 128), tm_x maps X [M, K] (box 64 x bn).  All 128-byte swizzled.

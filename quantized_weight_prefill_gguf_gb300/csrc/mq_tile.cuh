@@ -100,9 +100,14 @@ __device__ __forceinline__ UnitWalk unit_walk(const GemmArgs &a)
 // SCALED (the 8-bit path): every accumulator value is multiplied by its
 // weight row's scale and then by its token's scale, RN32(RN32(acc * sw) *
 // sx), before it is stored (partial planes too: the scaling is linear).
+//
+// tempty_rank >= 0 (2-SM MMAs): the accumulator is handed back on the
+// tempty barrier of CTA tempty_rank of the cluster (the MMA-issuing CTA),
+// which counts the epilogue warps of both CTAs.
 template <int BN, int NACC = 2, int NPART = 1, bool SCALED = false>
 __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, uint64_t *tfull, uint64_t *tempty,
-                                              volatile int *abort_flag, int warp, int lane, int kb_split = 1)
+                                              volatile int *abort_flag, int warp, int lane, int kb_split = 1,
+                                              int tempty_rank = -1)
 {
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -182,8 +187,12 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&tempty[acc]);
+        if (lane == 0) {
+            if (tempty_rank >= 0)
+                mbar_arrive_cluster(mapa_shared(&tempty[acc], static_cast<uint32_t>(tempty_rank)));
+            else
+                mbar_arrive(&tempty[acc]);
+        }
         if (++acc == NACC) {
             acc = 0;
             acc_phase ^= 1u;

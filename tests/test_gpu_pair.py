@@ -1,5 +1,5 @@
-"""CTA pairs (the default; MQ_PAIR=0 turns them off): clusters of two CTAs
-that share each token tile,
+"""Multicast CTA pairs (the default below 256-token tiles; MQ_PAIR=0 turns
+them off): clusters of two CTAs that share each token tile,
 multicast into both.  Every case runs with pairs on and off; both must
 match the oracle, and where the two plans split K the same way (no split)
 the outputs must agree bit for bit (each tile's arithmetic is unchanged).
@@ -20,9 +20,13 @@ def _mq():
 
 
 def _run(monkeypatch, pair, fn):
+    # MQ_2SM=0: 256-token tiles use the multicast pairs too (2-SM MMAs, the
+    # default there, have their own tests)
     monkeypatch.setenv("MQ_PAIR", "1" if pair else "0")
+    monkeypatch.setenv("MQ_2SM", "0")
     out = fn()
     monkeypatch.delenv("MQ_PAIR")
+    monkeypatch.delenv("MQ_2SM")
     return out
 
 
