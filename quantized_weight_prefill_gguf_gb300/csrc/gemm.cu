@@ -272,7 +272,7 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
 // ---------------------------------------------------------------- 2-SM MMAs
 // A CTA pair computes a 256 x BN tile with tcgen05.mma.cta_group::2: each
 // CTA stages its own 128 weight rows and half of the BN tokens (32 KB per
-// stage at BN = 256 instead of 48 KB), so shared memory holds seven stages
+// stage at BN = 256 instead of 48 KB), so shared memory holds six stages
 // instead of four and each byte in flight covers half again as much MMA
 // time (the single-CTA kernel's loads could not hide the L2 latency: its
 // tensor pipe idled 30 % of the time; the 7B gate GEMM goes 174 -> 163 us).  The
@@ -283,9 +283,14 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
 // even CTA's `tempty`.
 constexpr int kTwoSmAccs = 2;   // accumulators in TMEM (kTwoSmAccs * BN columns)
 
-template <int BN> struct Cfg2 {
+// Six stages (192 KB).  Seven fit (225.5 KB) and take the gate GEMM alone
+// from 164.8 to 163.3 us, but the layer step is the same within 0.2 %, and
+// they leave the SM ~2.5 KB of shared memory: too little for the next
+// kernel (the e4m3 step's activation quantization) to start beside the
+// GEMM's tail, which cost that step 28 us.
+template <int BN, bool F8 = false> struct Cfg2 {
     static constexpr int kHalfB = (BN / 2) * 128;   // this CTA's half of a token stage
-    static constexpr int kStages = 7;   // 5 / 6 / 7 measured 166.5 / 164.8 / 163.3 us on the gate
+    static constexpr int kStages = 6;
     static constexpr int kTmemCols = kTwoSmAccs * BN;
     static constexpr int kSmem = 1024 + kStages * (kABytes + kHalfB) + 512;
 };
@@ -293,7 +298,7 @@ template <int BN> struct Cfg2 {
 template <int BN, bool F8>
 __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorMap &tm_x, const GemmArgs &a)
 {
-    using C = Cfg2<BN>;
+    using C = Cfg2<BN, F8>;
     constexpr int kStep = F8 ? kBK8 : kBK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -531,7 +536,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 template <bool F8>
 cudaError_t launch_2sm(const WMaps &tw, const CUtensorMap &tx, const GemmArgs &a, const GemmPlan &p, cudaStream_t s)
 {
-    using C = Cfg2<256>;
+    using C = Cfg2<256, F8>;
     auto *kern = F8 ? k_gemm_e4m3_2sm<256> : k_gemm_cached_2sm<256>;
     static bool attr_done[64] = {};
     int dev = 0;
@@ -783,7 +788,7 @@ int pair_clusters_bn()
         return 0;
     if (cached[dev] != 0)
         return cached[dev] > 0 ? cached[dev] : 0;
-    const int smem = TWO_SM ? Cfg2<BN>::kSmem : Cfg<BN>::kSmem;
+    const int smem = TWO_SM ? Cfg2<BN, F8>::kSmem : Cfg<BN>::kSmem;
     auto *kern = TWO_SM ? (F8 ? k_gemm_e4m3_2sm<BN> : k_gemm_cached_2sm<BN>) : gemm_kernel<BN, F8, true>();
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
