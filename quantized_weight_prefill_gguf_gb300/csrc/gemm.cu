@@ -275,7 +275,7 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
 // stage at BN = 256 instead of 48 KB), so shared memory holds six stages
 // instead of four and each byte in flight covers half again as much MMA
 // time (the single-CTA kernel's loads could not hide the L2 latency: its
-// tensor pipe idled 30 % of the time; the 7B gate GEMM goes 174 -> 163 us).  The
+// tensor pipe idled 30 % of the time; the 7B gate GEMM goes 174 -> 165 us).  The
 // even CTA issues the MMAs; each D half lands in its own CTA's TMEM.
 // Barriers: each CTA's TMA completes its own `full`; the odd CTA relays that
 // to the even CTA's `peer_full`; the MMA commits arrive on `empty` and
