@@ -2,8 +2,9 @@
  * mq.h -- C ABI of the GB300 (sm_103a) quantized-weight prefill GEMM library.
  *
  * Computes the prefill matmul Y[M,N] = X[M,K] . W[N,K]^T where X is f16
- * activations, W is a GGUF block-quantized weight (Q4_K, Q6_K or Q8_0) and Y
- * is f32.  Two ways, both from the pages:
+ * activations, W is a GGUF weight (the block formats Q4_0, Q5_0, Q5_1, Q8_0,
+ * Q4_K, Q5_K, Q6_K, or the float types F32 / F16 / BF16) and Y is f32.  Two
+ * ways, both from the pages:
  *
  *   cached  W is decoded once, at registration, into a persistent f16 copy
  *           that a tensor-core GEMM then reads ("05 · 8p — Persistent f16
@@ -33,7 +34,28 @@
  *    and rounded once to nearest-even f16 (the dequant kernel of "05 · 8p",
  *    section 3.2: f32 product, then __float2half).  The cached and the fused
  *    paths decode to identical f16 values (section 3.3 Pitfalls: the same
- *    rounding path).
+ *    rounding path).  The other formats follow the same rule (their value
+ *    definitions are given with mq_type below).
+ *
+ * Environment switches (read on every call; tuning and diagnostics only,
+ * never needed for correct results):
+ *   MQ_M_GATE=n   mq_gemm_auto's token threshold (default 256).
+ *   MQ_PAIR=0     cached / e4m3 GEMMs without CTA pairs (default on: two CTAs
+ *                 of a cluster share each token tile).
+ *   MQ_2SM=0      256-token tiles as multicast CTA pairs instead of 2-SM MMAs
+ *                 (tcgen05.mma.cta_group::2, the default).
+ *   MQ_SPLITK=0   no split-K tail (default on).
+ *   MQ_BN=32|64|128|256   force the cached GEMM's token-tile width.
+ *   MQ_PDL=0      launch without programmatic dependent launch (default on).
+ *   MQ_KPAD=0|1   cache row padding never / always (default: the 2048-byte
+ *                 rule; the MQ_REG_* flags take precedence).
+ *   MQ_RAW_TMA=0  the fused path reads raw blocks by per-row bulk copies even
+ *                 when row tensor maps apply (at registration).
+ *   MQ_LOG=1      one line per registration and GEMM plan on stderr.
+ * Test-only failure injection (leave unset): MQ_FAULT_ALLOC=1 makes
+ * registration's cache allocation fail (MQ_ERR_OOM); MQ_INJECT_PRODUCER_STALL=1
+ * stops a GEMM's weight producer so its bounded waits time out (the kernel
+ * exits cleanly and mq_stream_status() reports MQ_ERR_DEVICE).
  */
 #ifndef MQ_H
 #define MQ_H
