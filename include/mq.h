@@ -37,8 +37,8 @@
  *    rounding path).  The other formats follow the same rule (their value
  *    definitions are given with mq_type below).
  *
- * Environment switches (read on every call; tuning and diagnostics only,
- * never needed for correct results):
+ * Environment switches (read on every call unless noted; tuning and
+ * diagnostics only, never needed for correct results):
  *   MQ_M_GATE=n   mq_gemm_auto's token threshold (default 256).
  *   MQ_PAIR=0     cached / e4m3 GEMMs without CTA pairs (default on: two CTAs
  *                 of a cluster share each token tile).
@@ -46,12 +46,14 @@
  *                 (tcgen05.mma.cta_group::2, the default).
  *   MQ_SPLITK=0   no split-K tail (default on).
  *   MQ_BN=32|64|128|256   force the cached GEMM's token-tile width.
- *   MQ_PDL=0      launch without programmatic dependent launch (default on).
+ *   MQ_PDL=0      launch without programmatic dependent launch (default on;
+ *                 read once, at the first launch).
  *   MQ_KPAD=0|1   cache row padding never / always (default: the 2048-byte
  *                 rule; the MQ_REG_* flags take precedence).
  *   MQ_RAW_TMA=0  the fused path reads raw blocks by per-row bulk copies even
  *                 when row tensor maps apply (at registration).
- *   MQ_LOG=1      one line per registration and GEMM plan on stderr.
+ *   MQ_LOG=1      one line per registration and GEMM plan on stderr (read
+ *                 once).
  * Test-only failure injection (leave unset): MQ_FAULT_ALLOC=1 makes
  * registration's cache allocation fail (MQ_ERR_OOM); MQ_INJECT_PRODUCER_STALL=1
  * stops a GEMM's weight producer so its bounded waits time out (the kernel
