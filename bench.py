@@ -687,12 +687,39 @@ def e4m3_layer(mq, torch, stream, weights, qdev, xdev, ys_f16, P, steps, flops_s
     mq.mq_stream_status()
     for h in hs:
         h.release()
-    return {"ms_per_step": ms, "tflops": flops_step / (ms * 1e-3) / 1e12, "steps": steps,
+    small = _e4m3_small_m(mq, torch, stream, weights[gi], qdev[gi], xdev, P)
+    return {"ms_per_step": ms, "tflops": flops_step / (ms * 1e-3) / 1e12, "steps": steps, "small_m": small,
             "kernel": {"name": "k_gemm_e4m3", "achieved_tflops": achieved, "peak_tflops": peak8,
                        "peak_note": "8-bit dense = 2 x the measured bf16 burst peak (the nominal fp8:bf16 ratio)",
                        "frac": achieved / peak8 if achieved else None},
             "rel_distance_to_f16_gate": dist,
             "note": "separate numeric contract: e4m3 operands with per-row / per-token f32 scales"}
+
+
+def _e4m3_small_m(mq, torch, stream, w, q, xdev, P):
+    """The e4m3 GEMM on the 7B gate shape at small M, where it streams one
+    byte per weight: back to back over R registered copies (> 400 MB of e4m3
+    weights touched), activations quantized once per M."""
+    wbytes = w.N * w.K + 4 * w.N
+    R = max(3, -(-(400 << 20) // wbytes))
+    qs = [q.clone() for _ in range(R)]
+    hs = [mq.mq_register_weight(w.qtype, qq, w.N, w.K, flags=mq.MQ_REG_E4M3) for qq in qs]
+    rows = []
+    for M in (1, 32, 128):
+        x8 = torch.empty((M, w.K), dtype=torch.uint8, device="cuda")
+        sx = torch.empty(M, dtype=torch.float32, device="cuda")
+        mq.mq_quantize_e4m3(xdev[w.K][:M], x8, sx, stream)
+        y = torch.empty((M, w.N), dtype=torch.float32, device="cuda")
+        t_us = _rotating_time_us(torch, [functools.partial(mq.mq_gemm_e4m3, x8, sx, h, y, M, stream) for h in hs],
+                                 stream)
+        byts = wbytes + M * w.K + 4 * M + 4 * M * w.N
+        rows.append({"M": M, "us": t_us, "gbs": byts / (t_us * 1e-6) / 1e9,
+                     "frac_hbm": byts / (t_us * 1e-6) / 1e9 / P["hbm_gbs"]})
+    mq.mq_stream_status()
+    for h in hs:
+        h.release()
+    del qs
+    return {"weight": f"{w.name} {w.N}x{w.K}", "copies": R, "rows": rows}
 
 
 def decode_steady(mq, torch, stream, P):
