@@ -1000,6 +1000,7 @@ int run_e4m3_group(const void *x8, const float *x_scale, const mq_handle *ws, fl
     a.qtype = w->type;
     a.pair = plan.pair;
     a.x_scale = x_scale;
+    a.stall_producer = env_int("MQ_INJECT_PRODUCER_STALL", 0) != 0 ? 1 : 0;   // failure injection (tests)
     a.groups = count;
     mq::WMaps maps{};
     int nt = 0;

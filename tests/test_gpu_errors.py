@@ -130,21 +130,32 @@ def test_dependent_chain_and_graph_capture(orc):
     assert torch.equal(y2, ref2)
 
 
-@pytest.mark.parametrize("path", ["cached", "fused"])
+@pytest.mark.parametrize("path", ["cached", "fused", "cached_2sm", "e4m3_2sm"])
 def test_bounded_wait_timeout_recovers(orc, monkeypatch, path):
     """A producer that never delivers (injected from the host): every
     consumer's bounded wait runs out after about a second, the kernel exits
-    cleanly (TMEM freed), mq_stream_status reports MQ_ERR_DEVICE, and the
-    context stays usable -- the next call is correct.  No GPU fault."""
+    cleanly (TMEM freed; both CTAs of a pair meet at the final cluster
+    barrier), mq_stream_status reports MQ_ERR_DEVICE, and the context stays
+    usable -- the next call is correct.  No GPU fault.  M = 48 runs the
+    multicast CTA pairs, M = 300 the 2-SM MMAs."""
     import time
     torch = torch_cuda()
     mq = _mq()
     g = synth.rng(12)
-    N, K, M = 256, 512, 48
+    N, K = 256, 512
+    M = 300 if path.endswith("2sm") else 48
     data = synth.weight_bytes(g, synth.Q4_K, N, K)
     x = dev(synth.activations(g, M, K))
-    h = mq.mq_register_weight(synth.Q4_K, dev(data), N, K)
-    fn = mq.mq_gemm if path == "cached" else mq.mq_gemm_fused
+    h = mq.mq_register_weight(synth.Q4_K, dev(data), N, K, flags=mq.MQ_REG_E4M3)
+    if path == "e4m3_2sm":
+        x8 = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+        sx = torch.empty(M, dtype=torch.float32, device="cuda")
+        mq.mq_quantize_e4m3(x, x8, sx)
+
+        def fn(_x, hh, yy, mm):
+            mq.mq_gemm_e4m3(x8, sx, hh, yy, mm)
+    else:
+        fn = mq.mq_gemm_fused if path == "fused" else mq.mq_gemm
     y = torch.zeros((M, N), dtype=torch.float32, device="cuda")
     mq.mq_stream_status()
     monkeypatch.setenv("MQ_INJECT_PRODUCER_STALL", "1")
@@ -158,5 +169,11 @@ def test_bounded_wait_timeout_recovers(orc, monkeypatch, path):
     mq.mq_stream_status()   # status word was cleared by the failing read
     fn(x, h, y, M)
     mq.mq_stream_status()
-    y_ref = orc.gemm_f64(x.cpu().numpy().view(np.uint16), orc.decode_matrix(synth.Q4_K, data, N, K))
+    if path == "e4m3_2sm":
+        codes, scales = h.e4m3_tensors()
+        y_ref = orc.gemm_e4m3_f64(x8.cpu().numpy(), sx.cpu().numpy(), codes.cpu().numpy()[:, :K],
+                                  scales.cpu().numpy())
+        del codes, scales
+    else:
+        y_ref = orc.gemm_f64(x.cpu().numpy().view(np.uint16), orc.decode_matrix(synth.Q4_K, data, N, K))
     assert_gemm_close(y.cpu().numpy(), y_ref, f"{path} after a timed-out call")
