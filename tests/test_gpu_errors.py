@@ -82,14 +82,16 @@ def test_forced_allocation_failure():
     assert second.strip() == "0"      # a cache-less registration allocates nothing and succeeds
 
 
-def test_dependent_chain_and_graph_capture(orc):
+@pytest.mark.parametrize("M", [64, 300])
+def test_dependent_chain_and_graph_capture(orc, M):
     """Two dependent GEMMs (the second consumes the first's output, cast to
     f16 on the device) with no host read in between, then the same pair
-    replayed from a CUDA graph after reserving the workspace."""
+    replayed from a CUDA graph after reserving the workspace.  M = 64 runs
+    the cached GEMM as multicast CTA pairs, M = 300 as 2-SM MMAs."""
     torch = torch_cuda()
     mq = _mq()
     g = synth.rng(8)
-    N1, K1, N2, M = 512, 1024, 256, 64
+    N1, K1, N2 = 512, 1024, 256
     d1 = synth.weight_bytes(g, synth.Q4_K, N1, K1)
     d2 = synth.weight_bytes(g, synth.Q6_K, N2, N1)
     x = synth.activations(g, M, K1)
