@@ -272,9 +272,9 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
 // ---------------------------------------------------------------- 2-SM MMAs
 // A CTA pair computes a 256 x BN tile with tcgen05.mma.cta_group::2: each
 // CTA stages its own 128 weight rows and half of the BN tokens (32 KB per
-// stage at BN = 256 instead of 48 KB), so shared memory holds six stages
-// instead of four and each byte in flight covers half again as much MMA
-// time (the single-CTA kernel's loads could not hide the L2 latency: its
+// K step at BN = 256 instead of 48 KB), so the same shared memory holds six
+// K steps instead of four and each byte in flight covers half again as much
+// MMA time (the single-CTA kernel's loads could not hide the L2 latency: its
 // tensor pipe idled 30 % of the time; the 7B gate GEMM goes 174 -> 165 us).  The
 // even CTA issues the MMAs; each D half lands in its own CTA's TMEM.
 // Barriers: each CTA's TMA completes its own `full`; the odd CTA relays that
@@ -283,16 +283,25 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
 // even CTA's `tempty`.
 constexpr int kTwoSmAccs = 2;   // accumulators in TMEM (kTwoSmAccs * BN columns)
 
-// Six stages (192 KB).  Seven fit (225.5 KB) and take the gate GEMM alone
-// from 164.8 to 163.3 us, but the layer step is the same within 0.2 %, and
-// they leave the SM ~2.5 KB of shared memory: too little for the next
-// kernel (the e4m3 step's activation quantization) to start beside the
-// GEMM's tail, which cost that step 28 us.
+// 192 KB of stages: three of two K steps each (64 KB per CTA).  With one K
+// step per stage (six of 32 KB) the single MMA-issuing thread, not the
+// tensor pipe, set the pace: a clock64 trace of the 7B gate GEMM showed a
+// steady 613 cycles per stage against 515 of MMA work (4 x 128.8), spent on
+// the two barrier waits, the commit and the loop.  Two K steps per stage
+// share that cost across eight MMAs: the layer step goes from 1463 to 1485
+// TFLOP/s (at a lower SM clock) and the e4m3 gate GEMM from 90.6 to 88.0 us.
+// A seventh 32 KB stage (225.5 KB) left the SM too little shared memory for
+// the next kernel (the e4m3 step's activation quantization) to start beside
+// the GEMM's tail, which cost that step 28 us.
+constexpr int kTwoSmSub = 2;   // K steps per pipeline stage
 template <int BN, bool F8 = false> struct Cfg2 {
-    static constexpr int kHalfB = (BN / 2) * 128;   // this CTA's half of a token stage
-    static constexpr int kStages = 6;
+    static constexpr int kHalfB = (BN / 2) * 128;   // this CTA's half of one K step's tokens
+    static constexpr int kSub = kTwoSmSub;
+    static constexpr int kStages = 6 / kSub;
+    static constexpr int kStageA = kSub * kABytes;
+    static constexpr int kStageB = kSub * kHalfB;
     static constexpr int kTmemCols = kTwoSmAccs * BN;
-    static constexpr int kSmem = 1024 + kStages * (kABytes + kHalfB) + 512;
+    static constexpr int kSmem = 1024 + kStages * (kStageA + kStageB) + 512;
 };
 
 template <int BN, bool F8>
@@ -303,8 +312,8 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = base;
-    uint8_t *sB = base + C::kStages * kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kHalfB);
+    uint8_t *sB = base + C::kStages * C::kStageA;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kStageB);
     uint64_t *peer_full = full + C::kStages;
     uint64_t *empty = peer_full + C::kStages;
     uint64_t *tfull = empty + C::kStages;
@@ -360,9 +369,12 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
                 tile_coords(a, ui.tile, nt, mt);
                 const int g = group_of(a, nt);
                 const int n0 = (nt - a.g_tile0[g]) * kTileRows;
-                for (int kb = ui.kb0; kb < ui.kb1 && pre < C::kStages; ++kb, ++pre) {
-                    mbar_arrive_expect_tx(&full[pre], kABytes + C::kHalfB);
-                    tma_load_2d(sA + pre * kABytes, &tm_w.m[g], &full[pre], kb * kStep, n0);
+                for (int kb = ui.kb0; kb < ui.kb1 && pre < C::kStages; kb += C::kSub, ++pre) {
+                    const int ns = min(C::kSub, ui.kb1 - kb);
+                    mbar_arrive_expect_tx(&full[pre], ns * (kABytes + C::kHalfB));
+                    for (int j = 0; j < ns; ++j)
+                        tma_load_2d(sA + pre * C::kStageA + j * kABytes, &tm_w.m[g], &full[pre], (kb + j) * kStep,
+                                    n0);
                     issued |= 1u << pre;
                 }
             }
@@ -376,9 +388,12 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
                 const CUtensorMap *tmw = &tm_w.m[g];
                 const int n0 = (nt - a.g_tile0[g]) * kTileRows;
                 const int m0 = mt * BN + static_cast<int>(rank) * (BN / 2);
-                for (int kb = ui.kb0; kb < ui.kb1; ++kb, ++step) {
+                for (int kb = ui.kb0; kb < ui.kb1; kb += C::kSub, ++step) {
+                    const int ns = min(C::kSub, ui.kb1 - kb);
                     if (step < pre) {
-                        tma_load_2d(sB + stage * C::kHalfB, &tm_x, &full[stage], kb * kStep, m0);
+                        for (int j = 0; j < ns; ++j)
+                            tma_load_2d(sB + stage * C::kStageB + j * C::kHalfB, &tm_x, &full[stage],
+                                        (kb + j) * kStep, m0);
                         if (++stage == C::kStages) {
                             stage = 0;
                             phase ^= 1u;
@@ -389,9 +404,12 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], kABytes + C::kHalfB);
-                    tma_load_2d(sA + stage * kABytes, tmw, &full[stage], kb * kStep, n0);
-                    tma_load_2d(sB + stage * C::kHalfB, &tm_x, &full[stage], kb * kStep, m0);
+                    mbar_arrive_expect_tx(&full[stage], ns * (kABytes + C::kHalfB));
+                    for (int j = 0; j < ns; ++j) {
+                        tma_load_2d(sA + stage * C::kStageA + j * kABytes, tmw, &full[stage], (kb + j) * kStep, n0);
+                        tma_load_2d(sB + stage * C::kStageB + j * C::kHalfB, &tm_x, &full[stage], (kb + j) * kStep,
+                                    m0);
+                    }
                     issued |= 1u << stage;
                     issue_parity = (issue_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) {
@@ -416,7 +434,7 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
             bool ok = true;
             for (int u = wk.first; ok && u < a.units; u += wk.stride) {
                 const UnitInfo ui = unit_info(a, u, wk.rank);
-                for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
+                for (int kb = ui.kb0; kb < ui.kb1; kb += C::kSub) {
                     if (!mbar_wait_bounded(&full[stage], phase, abort_flag, a.status)) {
                         ok = false;
                         break;
@@ -444,21 +462,28 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
-                for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
+                for (int kb = ui.kb0; kb < ui.kb1; kb += C::kSub) {
+                    const int ns = min(C::kSub, ui.kb1 - kb);
                     if (!mbar_wait_bounded(&full[stage], phase, abort_flag, a.status) ||
                         !mbar_wait_bounded(&peer_full[stage], phase, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * kABytes) >> 4);
-                    const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * C::kHalfB) >> 4);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        if constexpr (F8)
-                            umma_e4m3_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > ui.kb0 || k > 0) ? 1u : 0u);
-                        else
-                            umma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > ui.kb0 || k > 0) ? 1u : 0u);
+                    for (int j = 0; j < C::kSub; ++j) {
+                        if (j >= ns)
+                            break;
+                        const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * C::kStageA + j * kABytes) >> 4);
+                        const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * C::kStageB + j * C::kHalfB) >> 4);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t accum = (kb > ui.kb0 || j > 0 || k > 0) ? 1u : 0u;
+                            if constexpr (F8)
+                                umma_e4m3_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, accum);
+                            else
+                                umma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, accum);
+                        }
                     }
                     umma_commit_pair_mc(&empty[stage], 0x3);
                     if (++stage == C::kStages) {
