@@ -277,27 +277,38 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
 // MMA time (the single-CTA kernel's loads could not hide the L2 latency: its
 // tensor pipe idled 30 % of the time; the 7B gate GEMM goes 174 -> 165 us).  The
 // even CTA issues the MMAs; each D half lands in its own CTA's TMEM.
-// Barriers: each CTA's TMA completes its own `full`; the odd CTA relays that
-// to the even CTA's `peer_full`; the MMA commits arrive on `empty` and
-// `tfull` of both CTAs; both CTAs' epilogues release the accumulator on the
-// even CTA's `tempty`.
+// Barriers: the even CTA's producer expects both CTAs' bytes of a stage on
+// its own `full`, and the odd CTA's TMA copies complete there directly
+// (`cp.async.bulk.tensor ... .cta_group::2` takes the peer's barrier), so the
+// MMA issuer waits on one barrier per stage; the MMA commits arrive on
+// `empty` and `tfull` of both CTAs; both CTAs' epilogues release the
+// accumulator on the even CTA's `tempty`.
 constexpr int kTwoSmAccs = 2;   // accumulators in TMEM (kTwoSmAccs * BN columns)
 
-// 192 KB of stages: three of two K steps each (64 KB per CTA).  With one K
-// step per stage (six of 32 KB) the single MMA-issuing thread, not the
-// tensor pipe, set the pace: a clock64 trace of the 7B gate GEMM showed a
-// steady 613 cycles per stage against 515 of MMA work (4 x 128.8), spent on
-// the two barrier waits, the commit and the loop.  Two K steps per stage
-// share that cost across eight MMAs: the layer step goes from 1463 to 1485
-// TFLOP/s (at a lower SM clock) and the e4m3 gate GEMM from 90.6 to 88.0 us.
-// A seventh 32 KB stage (225.5 KB) left the SM too little shared memory for
-// the next kernel (the e4m3 step's activation quantization) to start beside
-// the GEMM's tail, which cost that step 28 us.
-constexpr int kTwoSmSub = 2;   // K steps per pipeline stage
+// Six stages of one K step (32 KB per CTA, 192 KB).  What the single
+// MMA-issuing thread spends per stage decides the depth: a clock64 trace of
+// the 7B gate GEMM (515 cycles of MMA work per K step, 4 x 128.8) showed it
+// busy ~613 cycles per stage when the odd CTA relayed its arrivals to a
+// second barrier (two waits, four MMAs, the commit, the loop), so the
+// pipeline ran at the issuer's pace.  Two K steps per stage (three 64 KB
+// stages) halved that cost but left a freed stage only two stages' MMA time
+// (~2060 cycles) to refill, against a load latency of 1580 cycles median and
+// 3140 at p90: the issuer then stalled on data.  With the odd CTA's copies
+// completing on the even CTA's barrier the issuer waits once per stage and
+// keeps up with one K step per stage, and five stages of slack (~2575
+// cycles) hide most of the latency: the 7B gate GEMM takes 159 us (161 with
+// two K steps per stage, 164.8 relayed with one), the e4m3 one 85.5 us.
+// A seventh stage (225.5 KB) gains 0.5 % on the gate GEMM alone but leaves
+// the SM too little shared memory for the next kernel (the e4m3 step's
+// activation quantization) to start beside the GEMM's tail, which cost that
+// step 28 us.  (An L2 prefetch of the weight tiles a few K steps ahead made
+// the loop slower: 163 -> 170 us.)
+constexpr int kTwoSmSlots = 6;   // 32 KB K-step slots of shared memory per CTA
+constexpr int kTwoSmSub = 1;     // K steps per pipeline stage
 template <int BN, bool F8 = false> struct Cfg2 {
     static constexpr int kHalfB = (BN / 2) * 128;   // this CTA's half of one K step's tokens
     static constexpr int kSub = kTwoSmSub;
-    static constexpr int kStages = 6 / kSub;
+    static constexpr int kStages = kTwoSmSlots / kSub;
     static constexpr int kStageA = kSub * kABytes;
     static constexpr int kStageB = kSub * kHalfB;
     static constexpr int kTmemCols = kTwoSmAccs * BN;
@@ -314,8 +325,7 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
     uint8_t *sA = base;
     uint8_t *sB = base + C::kStages * C::kStageA;
     uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kStageB);
-    uint64_t *peer_full = full + C::kStages;
-    uint64_t *empty = peer_full + C::kStages;
+    uint64_t *empty = full + C::kStages;
     uint64_t *tfull = empty + C::kStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
@@ -327,8 +337,7 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&peer_full[s], 1);
+            mbar_init(&full[s], 1);   // the even CTA's producer; both CTAs' bytes
             mbar_init(&empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -362,6 +371,17 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
             uint32_t phase = 0;
             uint32_t issued = 0, issue_parity = 0;
             bool ok = a.stall_producer == 0;
+            // The even CTA expects both CTAs' bytes of a stage on its own
+            // `full`; the odd CTA's copies complete there (.cta_group::2).
+            const bool odd = rank == 1;
+            const uint32_t full_even = mapa_shared(&full[0], 0);
+            constexpr uint32_t kStageTx = 2u * (kABytes + C::kHalfB);
+            auto load = [&](void *dst, const CUtensorMap *map, int st, int c0, int c1) {
+                if (odd)
+                    tma_load_2d_pair(dst, map, full_even + static_cast<uint32_t>(st) * 8u, c0, c1);
+                else
+                    tma_load_2d(dst, map, &full[st], c0, c1);
+            };
             int pre = 0;
             for (int u = wk.first; ok && pre < C::kStages && u < a.units; u += wk.stride) {
                 const UnitInfo ui = unit_info(a, u, wk.rank);
@@ -371,10 +391,10 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
                 const int n0 = (nt - a.g_tile0[g]) * kTileRows;
                 for (int kb = ui.kb0; kb < ui.kb1 && pre < C::kStages; kb += C::kSub, ++pre) {
                     const int ns = min(C::kSub, ui.kb1 - kb);
-                    mbar_arrive_expect_tx(&full[pre], ns * (kABytes + C::kHalfB));
+                    if (!odd)
+                        mbar_arrive_expect_tx(&full[pre], ns * kStageTx);
                     for (int j = 0; j < ns; ++j)
-                        tma_load_2d(sA + pre * C::kStageA + j * kABytes, &tm_w.m[g], &full[pre], (kb + j) * kStep,
-                                    n0);
+                        load(sA + pre * C::kStageA + j * kABytes, &tm_w.m[g], pre, (kb + j) * kStep, n0);
                     issued |= 1u << pre;
                 }
             }
@@ -392,8 +412,7 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
                     const int ns = min(C::kSub, ui.kb1 - kb);
                     if (step < pre) {
                         for (int j = 0; j < ns; ++j)
-                            tma_load_2d(sB + stage * C::kStageB + j * C::kHalfB, &tm_x, &full[stage],
-                                        (kb + j) * kStep, m0);
+                            load(sB + stage * C::kStageB + j * C::kHalfB, &tm_x, stage, (kb + j) * kStep, m0);
                         if (++stage == C::kStages) {
                             stage = 0;
                             phase ^= 1u;
@@ -404,11 +423,11 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], ns * (kABytes + C::kHalfB));
+                    if (!odd)
+                        mbar_arrive_expect_tx(&full[stage], ns * kStageTx);
                     for (int j = 0; j < ns; ++j) {
-                        tma_load_2d(sA + stage * C::kStageA + j * kABytes, tmw, &full[stage], (kb + j) * kStep, n0);
-                        tma_load_2d(sB + stage * C::kStageB + j * C::kHalfB, &tm_x, &full[stage], (kb + j) * kStep,
-                                    m0);
+                        load(sA + stage * C::kStageA + j * kABytes, tmw, stage, (kb + j) * kStep, n0);
+                        load(sB + stage * C::kStageB + j * C::kHalfB, &tm_x, stage, (kb + j) * kStep, m0);
                     }
                     issued |= 1u << stage;
                     issue_parity = (issue_parity & ~(1u << stage)) | (phase << stage);
@@ -420,33 +439,25 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
             }
             if (!ok) {
                 volatile int no_abort = 0;
-                for (int s = 0; s < C::kStages; ++s)
-                    if (issued & (1u << s))
-                        mbar_wait_bounded(&full[s], (issue_parity >> s) & 1u, &no_abort, a.status);
+                if (odd) {
+                    // This CTA's copies complete on the even CTA's barriers, which
+                    // it cannot wait on: give any still in flight 200 us to land
+                    // (the even CTA's own drain, before the final cluster barrier,
+                    // covers every stage both CTAs issued).
+                    if (issued) {
+                        const uint64_t t0 = globaltimer_ns();
+                        while (globaltimer_ns() - t0 < 200000ull)
+                            __nanosleep(1000);
+                    }
+                } else {
+                    for (int s = 0; s < C::kStages; ++s)
+                        if (issued & (1u << s))
+                            mbar_wait_bounded(&full[s], (issue_parity >> s) & 1u, &no_abort, a.status);
+                }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 1) {
-            // ---------------- relay: this CTA's stage landed -> the even CTA's peer_full
-            const uint32_t peer_full0 = mapa_shared(&peer_full[0], 0);
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int u = wk.first; ok && u < a.units; u += wk.stride) {
-                const UnitInfo ui = unit_info(a, u, wk.rank);
-                for (int kb = ui.kb0; kb < ui.kb1; kb += C::kSub) {
-                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, a.status)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_cluster(peer_full0 + static_cast<uint32_t>(stage) * 8u);
-                    if (++stage == C::kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-        } else if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             // ---------------- MMA issuer (even CTA): M = 256 across the pair
             constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(2 * kTileRows, BN) : idesc_f16_f32(2 * kTileRows, BN);
             const uint64_t a_desc0 = sdesc_k_sw128(smem_u32(sA));
@@ -464,8 +475,7 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
                 for (int kb = ui.kb0; kb < ui.kb1; kb += C::kSub) {
                     const int ns = min(C::kSub, ui.kb1 - kb);
-                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, a.status) ||
-                        !mbar_wait_bounded(&peer_full[stage], phase, abort_flag, a.status)) {
+                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }

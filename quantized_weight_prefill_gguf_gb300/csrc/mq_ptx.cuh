@@ -128,6 +128,19 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// 2-D tiled load into this CTA's shared memory whose bytes complete on the
+// mbarrier at shared::cluster address `bar`: with .cta_group::2 that barrier
+// may be the peer CTA's (the other CTA of this CTA's pair).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t bar, int32_t c0,
+                                                 int32_t c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 // 2-D tiled load multicast to the CTAs of `mask` in this CTA's cluster: the
 // box lands at the same shared-memory offset in each of them and completes
 // bytes on the mbarrier at the same offset in each.
@@ -323,10 +336,10 @@ __device__ __forceinline__ uint32_t mapa_shared(const void *p, uint32_t rank)
 // Arrive on an mbarrier given by its shared::cluster address (in this CTA
 // or its peer), with the default release semantics at CTA scope.  The
 // arrivals this is used for order no ordinary memory across the CTAs: they
-// relay TMA completions (tracked by the barrier's transaction count) and hand
-// back TMEM after tcgen05.wait::ld and the tcgen05 thread-sync fences.  A
-// cluster-scope release here costs a cluster-wide memory fence per arrival
-// (measured: it throttled the per-stage relay to ~0.9 us).
+// hand back TMEM after tcgen05.wait::ld and the tcgen05 thread-sync fences.
+// A cluster-scope release here costs a cluster-wide memory fence per arrival
+// (measured when it also relayed each pipeline stage of the 2-SM GEMM: it
+// throttled every stage to ~0.9 us).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
