@@ -339,7 +339,6 @@ int mq_debug_schedule(int64_t M, int64_t N, int64_t K, int sms, int path, int pa
                       int32_t *units, int64_t cap, int64_t *count);
 
 /*
- * mq_gemm_noalloc -- the cached GEMM/*
  * mq_gemm_noalloc -- the cached GEMM (same result as mq_gemm, same
  * arguments) for callers that cannot allocate device memory: code that runs
  * while a stream is captured into a CUDA graph in global capture mode (where
