@@ -26,7 +26,8 @@ Printed: one JSON line (rank 0) with the contract keys plus
                 fused and cached at M = 32 and 2048, same method;
   triangle      the 7B layer's seven GEMMs one call each through the cached
                 path, the per-call scratch mode and the fused path at M = 32
-                and 2048: time per layer and device bytes each mode holds;
+                and 2048 (and the fused path grouped as q|k|v, o, gate|up,
+                down): time per layer and device bytes each mode holds;
   row_pad       F16 / BF16 weights of the Llama-3.1-8B layer's shapes at
                 M = 512, cached GEMM on the row-padded copy vs unpadded rows;
   e4m3          the same layer step through the 8-bit variant (its own
@@ -574,7 +575,9 @@ def triangle(mq, torch, stream, weights, handles, qdev, xs):
     GEMMs as its own call (no grouping) through the cached path (resident
     f16 caches), the per-call scratch mode (one f16 scratch as large as the
     largest weight, re-decoded every call) and the fused path (raw blocks
-    only).  Time per layer = the seven calls back to back, median of 5."""
+    only), and the fused path once more in the layer's four launch groups
+    (q|k|v and gate|up as one mq_gemm_fused_grouped call each).  Time per
+    layer = the calls back to back, median of 5."""
     fused_h = [mq.mq_register_weight(w.qtype, q, w.N, w.K, flags=mq.MQ_REG_NO_CACHE)
                for w, q in zip(weights, qdev)]
     scratch_elems = max(w.N * h.info()[2] for w, h in zip(weights, handles))
@@ -592,6 +595,9 @@ def triangle(mq, torch, stream, weights, handles, qdev, xs):
                         for w, h, y in zip(weights, handles, ys)],
             "fused": [functools.partial(mq.mq_gemm_fused, xm[w.K], h, y, M, stream)
                       for w, h, y in zip(weights, fused_h, ys)],
+            "fused_grouped": [functools.partial(mq.mq_gemm_fused_grouped, xm[weights[idx[0]].K],
+                                                [fused_h[i] for i in idx], [ys[i] for i in idx], M, stream)
+                              for idx in ([i for i, w in enumerate(weights) if w.name in grp] for grp in LAUNCH_GROUPS)],
         }
         row = {"M": M}
         for name, calls in modes.items():
@@ -602,7 +608,8 @@ def triangle(mq, torch, stream, weights, handles, qdev, xs):
         h.release()
     return {"rows": rows, "device_bytes": {"cached": raw_bytes + cache_bytes,
                                            "scratch": raw_bytes + 2 * scratch_elems, "fused": raw_bytes},
-            "method": "seven single calls back to back (layer weights 148 MB raw / 466 MB f16, > L2)"}
+            "method": "seven single calls back to back (layer weights 148 MB raw / 466 MB f16, > L2); "
+                      "fused_grouped: four calls (q|k|v and gate|up through mq_gemm_fused_grouped)"}
 
 
 def row_pad(mq, torch, stream):

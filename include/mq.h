@@ -229,6 +229,30 @@ int mq_gemm_fused(const void *x, mq_handle w, float *y, int64_t M, void *stream)
 int mq_gemm_grouped(const void *x, const mq_handle *w, int count, float *const *y, int64_t M, void *stream);
 
 /*
+ * mq_gemm_fused_grouped -- the fused path for `count` (1..4) weights that
+ * share K and X, in one launch: y[g][M, N_g] = X . W_g^T, every member's raw
+ * blocks decoded on chip as in mq_gemm_fused (the same f16 values as the
+ * cache).  The shared-input batch of mq_gemm_grouped ("Eager GPU Offload
+ * Without A Compute Graph", section "Storage and transfer reuse") on the
+ * raw-block path: at small M, where each fused launch pays a fixed ramp-up
+ * of its weight stream, q|k|v or gate|up then pay it once.
+ *
+ * Arguments: as mq_gemm_grouped, but the handles need no f16 cache
+ * (MQ_REG_NO_CACHE is fine) and all members have the same block format.
+ * One launch when every N_g is a multiple of 128 (plus one split-K
+ * reduction when the last wave is split); otherwise the members run one
+ * after another with mq_gemm_fused.  Float weights (F32/F16/BF16) have
+ * nothing to decode: the call is then mq_gemm_grouped.  The outputs equal
+ * what mq_gemm_fused computes for each member, up to f32 summation order.
+ * Errors: MQ_ERR_INVALID (w or y NULL, count out of range, stale handle,
+ * members on different devices or of different types), MQ_ERR_SHAPE (K
+ * differs, bad M, the fused path's K and stream-length conditions),
+ * MQ_ERR_ALIGN, MQ_ERR_OOM (split-K workspace), MQ_ERR_CUDA.  Nothing is
+ * launched when an argument check fails.
+ */
+int mq_gemm_fused_grouped(const void *x, const mq_handle *w, int count, float *const *y, int64_t M, void *stream);
+
+/*
  * mq_gemm_auto -- M gate: fused when M < gate (and the handle allows it),
  * cached otherwise ("ggml-cuda: GEMM weight row padding ...", Summary: the
  * f16 path is a large-batch win; the threshold is a token count per call).

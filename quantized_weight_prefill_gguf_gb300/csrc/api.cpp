@@ -334,13 +334,17 @@ int run_gemm_group(const void *x, const mq_handle *ws, float *const *ys, int cou
     a.pair = plan.pair;
     a.groups = count;
     mq::WMaps maps{};
+    mq::RawMapsG raw{};
     int nt = 0;
     for (int g = 0; g < count; ++g) {
         a.g_tile0[g] = nt;
         a.g_y[g] = ys[g];
         a.g_N[g] = ws[g]->N;
+        a.g_wq[g] = ws[g]->qdata;
         nt += static_cast<int>((ws[g]->N + 127) / 128);
-        if (!fused)
+        if (fused)
+            raw.w[g] = ws[g]->raw_maps;
+        else
             maps.m[g] = ws[g]->tm_cache;
     }
     a.g_tile0[count] = nt;
@@ -358,7 +362,7 @@ int run_gemm_group(const void *x, const mq_handle *ws, float *const *ys, int cou
     // kernel's bounded waits run out (about 1 s), it exits cleanly and
     // mq_stream_status() reports MQ_ERR_DEVICE.
     a.stall_producer = env_int("MQ_INJECT_PRODUCER_STALL", 0) != 0 ? 1 : 0;
-    cudaError_t e = fused ? mq::launch_gemm_fused(tm_x, w->raw_maps, a, plan, s)
+    cudaError_t e = fused ? mq::launch_gemm_fused(tm_x, raw, a, plan, s)
                           : mq::launch_gemm_cached(maps, tm_x, a, plan, s);
     if (e != cudaSuccess)
         return cuda_fail(e, fused ? "fused GEMM launch" : "cached GEMM launch");
@@ -841,6 +845,54 @@ int mq_gemm_fused(const void *x, mq_handle w, float *y, int64_t M, void *stream)
         return fail(MQ_ERR_SHAPE, "fused path needs the block stream length (%lld bytes) to be a multiple of 16",
                     (long long)(w->nblocks * w->bb));
     return run_gemm(x, w, y, M, static_cast<cudaStream_t>(stream), true);
+}
+
+int mq_gemm_fused_grouped(const void *x, const mq_handle *w, int count, float *const *y, int64_t M, void *stream)
+{
+    if (!w || !y)
+        return fail(MQ_ERR_INVALID, "%s is NULL", w ? "y" : "w");
+    if (count < 1 || count > mq::kMaxGroup)
+        return fail(MQ_ERR_INVALID, "count=%d: need 1 <= count <= %d", count, mq::kMaxGroup);
+    bool one_launch = true;
+    for (int g = 0; g < count; ++g) {
+        int rc = check_gemm_args(x, w[g], y[g], M);
+        if (rc)
+            return rc;
+        if (w[g]->K != w[0]->K)
+            return fail(MQ_ERR_SHAPE, "member %d has K=%lld, member 0 has K=%lld: a group shares X", g,
+                        (long long)w[g]->K, (long long)w[0]->K);
+        if (w[g]->type != w[0]->type)
+            return fail(MQ_ERR_INVALID, "member %d has type %d, member 0 has type %d: a fused group decodes one format",
+                        g, w[g]->type, w[0]->type);
+        if (w[g]->device != w[0]->device)
+            return fail(MQ_ERR_INVALID, "member %d is registered on device %d, member 0 on %d", g, w[g]->device,
+                        w[0]->device);
+        if (w[g]->raw_g != w[0]->raw_g)
+            one_launch = false;
+        if (w[g]->N % 128 != 0)
+            one_launch = false;
+    }
+    if (is_float_type(w[0]->type))   // nothing to decode on chip: the f16 operands exist
+        return mq_gemm_grouped(x, w, count, y, M, stream);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!one_launch || count == 1) {
+        // A member whose N is not a multiple of the 128-row tile would share a
+        // tile with the next one: run the members one after another instead.
+        for (int g = 0; g < count; ++g) {
+            int rc = mq_gemm_fused(x, w[g], y[g], M, stream);
+            if (rc)
+                return rc;
+        }
+        return MQ_OK;
+    }
+    if (w[0]->K % 64 != 0)
+        return fail(MQ_ERR_SHAPE, "fused path needs K %% 64 == 0 (K=%lld)", (long long)w[0]->K);
+    for (int g = 0; g < count; ++g)
+        if (w[g]->raw_g == 0 && (w[g]->nblocks * w[g]->bb) % 16 != 0)
+            return fail(MQ_ERR_SHAPE,
+                        "fused path needs member %d's block stream length (%lld bytes) to be a multiple of 16", g,
+                        (long long)(w[g]->nblocks * w[g]->bb));
+    return run_gemm_group(x, w, y, count, M, s, true);
 }
 
 int mq_gemm_auto(const void *x, mq_handle w, float *y, int64_t M, void *stream)

@@ -440,7 +440,7 @@ MQ_SMALL_STEP(7)
 
 template <int BN, int QT, bool TMA_RAW>
 __global__ void __launch_bounds__(kThreadsF, 1)
-    k_gemm_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ RawMaps maps, const GemmArgs a)
+    k_gemm_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ RawMapsG maps, const GemmArgs a)
 {
     using F = QF<QT>;
     constexpr int kXSub = BN * kBK * 2;               // one 64-wide K step of activations
@@ -500,8 +500,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     if (warp == 2 && lane == 0) {
         prefetch_tensormap(&tm_x);
         if (TMA_RAW)
-            for (int c = 0; c < g; ++c)
-                prefetch_tensormap(&maps.m[c]);
+            for (int gm = 0; gm < a.groups; ++gm)
+                for (int c = 0; c < g; ++c)
+                    prefetch_tensormap(&maps.w[gm].m[c]);
     }
     tc_fence_before();
     __syncthreads();
@@ -518,7 +519,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         bool ok = a.stall_producer == 0;
         for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
             const UnitInfo ui = unit_info(a, u);
-            const int64_t n0 = static_cast<int64_t>(ui.tile / a.m_tiles) * kTileRows;
+            const int nt = ui.tile / a.m_tiles;
+            const int gm = group_of(a, nt);   // member of a group; rows counted inside it
+            const int64_t n0 = static_cast<int64_t>(nt - a.g_tile0[gm]) * kTileRows;
             for (int kb = ui.kb0; kb < ui.kb1; kb += kChunkSteps) {
                 const int steps = ui.kb1 - kb < kChunkSteps ? ui.kb1 - kb : kChunkSteps;
                 bool w = true;
@@ -537,7 +540,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                         for (int c = 0; c < g; ++c) {
                             const int mis = static_cast<int>((c * a.raw_rb) & 15);
                             const int x0 = static_cast<int>(((mis + ob) & ~static_cast<int64_t>(15)) >> 1);
-                            tma_load_2d(slot + static_cast<size_t>(c) * rows_per_class * RS, &maps.m[c],
+                            tma_load_2d(slot + static_cast<size_t>(c) * rows_per_class * RS, &maps.w[gm].m[c],
                                         &raw_full[r], x0, static_cast<int32_t>(n0 / g));
                         }
                     }
@@ -547,7 +550,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int64_t n = n0 + lane + 32 * i;
-                        if (n < a.N) {
+                        if (n < a.g_N[gm]) {
                             sp[i] = row_span<QT>(n, a.K, static_cast<int64_t>(kb) * kBK,
                                                  static_cast<int64_t>(steps) * kBK);
                             total += sp[i].bytes;
@@ -565,7 +568,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         if (sp[i].bytes)
-                            bulk_load(slot + static_cast<size_t>(lane + 32 * i) * RS, a.wq + sp[i].s0, sp[i].bytes,
+                            bulk_load(slot + static_cast<size_t>(lane + 32 * i) * RS, a.g_wq[gm] + sp[i].s0, sp[i].bytes,
                                       &raw_full[r]);
                 }
                 issued |= 1u << r;
@@ -730,8 +733,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         bool ok = true;
         for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
             const UnitInfo ui = unit_info(a, u);
-            const int64_t n = static_cast<int64_t>(ui.tile / a.m_tiles) * kTileRows + row;
-            const bool valid = n < a.N;
+            const int nt = ui.tile / a.m_tiles;
+            const int gm = group_of(a, nt);
+            const int64_t n = static_cast<int64_t>(nt - a.g_tile0[gm]) * kTileRows + row;   // row inside member gm
+            const bool valid = n < a.g_N[gm];
             // Tensor-map path: the slot row of a chunk starts at the 16-byte
             // boundary at or below the chunk's first byte, so the chunk sits
             // lead = (mis + ob) % 16 bytes into it, where mis is the row's
@@ -882,7 +887,7 @@ FusedLayout fused_layout(int qt, int bn, bool tma_raw)
 }
 
 template <int BN, int QT, bool TMA_RAW>
-cudaError_t launch_f(const CUtensorMap &tx, const RawMaps &maps, const GemmArgs &a0, const GemmPlan &p,
+cudaError_t launch_f(const CUtensorMap &tx, const RawMapsG &maps, const GemmArgs &a0, const GemmPlan &p,
                      cudaStream_t s)
 {
     const FusedLayout L = fused_layout(QT, BN, TMA_RAW);
@@ -912,7 +917,7 @@ cudaError_t launch_f(const CUtensorMap &tx, const RawMaps &maps, const GemmArgs 
 }
 
 template <int QT, bool TMA_RAW>
-cudaError_t launch_q(const CUtensorMap &tx, const RawMaps &maps, const GemmArgs &a, const GemmPlan &p,
+cudaError_t launch_q(const CUtensorMap &tx, const RawMapsG &maps, const GemmArgs &a, const GemmPlan &p,
                      cudaStream_t s)
 {
     switch (p.bn) {
@@ -976,7 +981,7 @@ int encode_raw_maps(RawMaps *maps, const void *qdata, int type, int64_t N, int64
     return g;
 }
 
-cudaError_t launch_gemm_fused(const CUtensorMap &tx, const RawMaps &maps, const GemmArgs &a, const GemmPlan &p,
+cudaError_t launch_gemm_fused(const CUtensorMap &tx, const RawMapsG &maps, const GemmArgs &a, const GemmPlan &p,
                               cudaStream_t s)
 {
     if (a.K % kBK != 0 || p.kb_align != kChunkSteps)

@@ -40,7 +40,7 @@ struct GemmArgs {
     float *y;            // [M, N] f32 output
     float *ws;           // split-K partial planes: [slot][part][BN][128]
     unsigned *status;    // device status word
-    const uint8_t *wq;   // raw quantized stream (fused path)
+    const uint8_t *wq;   // raw quantized stream of member 0 (fused path)
     int64_t M, N, K;
     int m_tiles, n_tiles;
     int kblocks;         // ceil(K / 64)
@@ -63,6 +63,7 @@ struct GemmArgs {
     int groups;                     // members of the group (1 for a single weight)
     int g_tile0[kMaxGroup + 1];     // first n-tile of each member; g_tile0[groups] = n_tiles
     float *g_y[kMaxGroup];          // member outputs
+    const uint8_t *g_wq[kMaxGroup]; // fused path: member raw streams
     int64_t g_N[kMaxGroup];         // member row counts
 };
 
@@ -89,6 +90,12 @@ struct WMaps {
 constexpr int kMaxRawMaps = 8;
 struct RawMaps {
     CUtensorMap m[kMaxRawMaps];
+};
+
+// Raw-block tensor maps of the members of a fused group (one for a single
+// weight); every member has the same type and K, so the same row classes.
+struct RawMapsG {
+    RawMaps w[kMaxGroup];
 };
 
 struct GemmPlan {
@@ -146,7 +153,7 @@ cudaError_t launch_quant_e4m3(const __half *src, int64_t rows, int64_t K, int64_
 
 // Fused path: tm_x as above; the weight is read from a.wq, through `maps`
 // when a.raw_g > 0.
-cudaError_t launch_gemm_fused(const CUtensorMap &tm_x, const RawMaps &maps, const GemmArgs &a, const GemmPlan &p,
+cudaError_t launch_gemm_fused(const CUtensorMap &tm_x, const RawMapsG &maps, const GemmArgs &a, const GemmPlan &p,
                               cudaStream_t s);
 
 // Build the raw-weight tensor maps of a block-aligned weight; returns g (0
