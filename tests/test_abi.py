@@ -64,6 +64,15 @@ def test_host_validation_without_device(lib):
     assert lib.mq_release_weight(ctypes.c_void_p(0x1234)) == -1
     assert lib.mq_set_m_gate(0) == -1
     assert lib.mq_reserve_workspace(-1) == -1
+    # grouped entry points: null arrays, count out of range, stale member handles
+    P = ctypes.c_void_p
+    ys = (P * 2)(16, 32)
+    for fn in (lib.mq_gemm_grouped, lib.mq_gemm_fused_grouped):
+        assert fn(P(16), None, 2, ys, 8, None) == -1
+        assert fn(P(16), (P * 2)(0x1234, 0x1234), 2, None, 8, None) == -1
+        assert fn(P(16), (P * 2)(0x1234, 0x1234), 0, ys, 8, None) == -1
+        assert fn(P(16), (P * 2)(0x1234, 0x1234), 5, ys, 8, None) == -1
+        assert fn(P(16), (P * 2)(0x1234, 0x1234), 2, ys, 8, None) == -1
 
 
 def test_product_and_oracle_share_nothing():
