@@ -253,6 +253,17 @@ int mq_gemm_grouped(const void *x, const mq_handle *w, int count, float *const *
 int mq_gemm_fused_grouped(const void *x, const mq_handle *w, int count, float *const *y, int64_t M, void *stream);
 
 /*
+ * mq_gemm_auto_grouped -- the M gate of mq_gemm_auto for a group: below the
+ * gate (mq_get_m_gate()), when every member can take the fused path (one
+ * block format, the fused path's K and stream-length conditions), the call
+ * is mq_gemm_fused_grouped; at and above it mq_gemm_grouped.  A member
+ * registered without an f16 cache sends the whole group to
+ * mq_gemm_fused_grouped.  Arguments, results and errors: those of the call
+ * it makes.
+ */
+int mq_gemm_auto_grouped(const void *x, const mq_handle *w, int count, float *const *y, int64_t M, void *stream);
+
+/*
  * mq_gemm_auto -- M gate: fused when M < gate (and the handle allows it),
  * cached otherwise ("ggml-cuda: GEMM weight row padding ...", Summary: the
  * f16 path is a large-batch win; the threshold is a token count per call).

@@ -27,7 +27,7 @@ STATUS = {0: "MQ_OK", -1: "MQ_ERR_INVALID", -2: "MQ_ERR_UNSUPPORTED_TYPE", -3: "
 EXPORTS = ("mq_register_weight", "mq_release_weight", "mq_weight_info", "mq_dequantize", "mq_gemm",
            "mq_gemm_fused", "mq_gemm_auto", "mq_get_m_gate", "mq_set_m_gate", "mq_reserve_workspace",
            "mq_stream_status", "mq_launch_count", "mq_error_string", "mq_last_error_detail", "mq_version",
-           "mq_trace_enable", "mq_trace_count", "mq_trace_read", "mq_gemm_noalloc", "mq_gemm_grouped", "mq_gemm_fused_grouped",
+           "mq_trace_enable", "mq_trace_count", "mq_trace_read", "mq_gemm_noalloc", "mq_gemm_grouped", "mq_gemm_fused_grouped", "mq_gemm_auto_grouped",
            "mq_gemm_scratch", "mq_quantize_e4m3", "mq_gemm_e4m3", "mq_weight_e4m3_info",
            "mq_gemm_e4m3_grouped", "mq_debug_schedule")
 MQ_TRACE_GEMM_CACHED, MQ_TRACE_GEMM_FUSED, MQ_TRACE_DECODE = 1, 2, 3
@@ -64,6 +64,7 @@ def _load() -> ctypes.CDLL:
         "mq_weight_e4m3_info": ([_P, ctypes.POINTER(_I64), ctypes.POINTER(_P), ctypes.POINTER(_P)], ctypes.c_int),
         "mq_gemm_grouped": ([_P, ctypes.POINTER(_P), ctypes.c_int, ctypes.POINTER(_P), _I64, _P], ctypes.c_int),
         "mq_gemm_fused_grouped": ([_P, ctypes.POINTER(_P), ctypes.c_int, ctypes.POINTER(_P), _I64, _P], ctypes.c_int),
+        "mq_gemm_auto_grouped": ([_P, ctypes.POINTER(_P), ctypes.c_int, ctypes.POINTER(_P), _I64, _P], ctypes.c_int),
         "mq_debug_schedule": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _I64, _P],
                               ctypes.c_int),
         "mq_get_m_gate": ([], _I64),
@@ -237,6 +238,17 @@ def mq_gemm_fused_grouped(x, ws, ys, M: int | None = None, stream=None) -> None:
     yarr = (_P * n)(*[_ptr(y) for y in ys])
     _check(_lib().mq_gemm_fused_grouped(_ptr(x), harr, n, yarr, M if M is not None else x.shape[0],
                                         _stream(stream)), "mq_gemm_fused_grouped")
+
+
+def mq_gemm_auto_grouped(x, ws, ys, M: int | None = None, stream=None) -> None:
+    """The M gate for a group: mq_gemm_fused_grouped below it, mq_gemm_grouped at and above it."""
+    if len(ws) != len(ys):
+        raise ValueError(f"{len(ws)} weights but {len(ys)} outputs")
+    n = len(ws)
+    harr = (_P * n)(*[w.handle for w in ws])
+    yarr = (_P * n)(*[_ptr(y) for y in ys])
+    _check(_lib().mq_gemm_auto_grouped(_ptr(x), harr, n, yarr, M if M is not None else x.shape[0],
+                                       _stream(stream)), "mq_gemm_auto_grouped")
 
 
 def mq_gemm_noalloc(x, w: Weight, y, M: int | None = None, stream=None) -> None:

@@ -895,6 +895,26 @@ int mq_gemm_fused_grouped(const void *x, const mq_handle *w, int count, float *c
     return run_gemm_group(x, w, y, count, M, s, true);
 }
 
+int mq_gemm_auto_grouped(const void *x, const mq_handle *w, int count, float *const *y, int64_t M, void *stream)
+{
+    if (!w || !y)
+        return fail(MQ_ERR_INVALID, "%s is NULL", w ? "y" : "w");
+    if (count < 1 || count > mq::kMaxGroup)
+        return fail(MQ_ERR_INVALID, "count=%d: need 1 <= count <= %d", count, mq::kMaxGroup);
+    bool all_cached = true, fused_ok = true;
+    for (int g = 0; g < count; ++g) {
+        int rc = check_handle(w[g]);
+        if (rc)
+            return rc;
+        all_cached = all_cached && w[g]->cache != nullptr;
+        fused_ok = fused_ok && !is_float_type(w[g]->type) && w[g]->type == w[0]->type && w[g]->K % 64 == 0 &&
+                   (w[g]->raw_g > 0 || (w[g]->nblocks * w[g]->bb) % 16 == 0);
+    }
+    if (!all_cached || (M < current_gate() && fused_ok))
+        return mq_gemm_fused_grouped(x, w, count, y, M, stream);
+    return mq_gemm_grouped(x, w, count, y, M, stream);
+}
+
 int mq_gemm_auto(const void *x, mq_handle w, float *y, int64_t M, void *stream)
 {
     int rc = check_gemm_args(x, w, y, M);

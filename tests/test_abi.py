@@ -67,7 +67,7 @@ def test_host_validation_without_device(lib):
     # grouped entry points: null arrays, count out of range, stale member handles
     P = ctypes.c_void_p
     ys = (P * 2)(16, 32)
-    for fn in (lib.mq_gemm_grouped, lib.mq_gemm_fused_grouped):
+    for fn in (lib.mq_gemm_grouped, lib.mq_gemm_fused_grouped, lib.mq_gemm_auto_grouped):
         assert fn(P(16), None, 2, ys, 8, None) == -1
         assert fn(P(16), (P * 2)(0x1234, 0x1234), 2, None, 8, None) == -1
         assert fn(P(16), (P * 2)(0x1234, 0x1234), 0, ys, 8, None) == -1

@@ -168,3 +168,36 @@ def test_fused_group_errors():
     mq.mq_stream_status()
     for h in (ha, hb, hc):
         h.release()
+
+
+def test_auto_grouped_gate(orc):
+    """mq_gemm_auto_grouped: one fused launch below the gate, the grouped
+    cached GEMM at and above it (seen in the launch trace); a member without
+    an f16 cache sends the group to the fused path at any M."""
+    torch = torch_cuda()
+    mq = _mq()
+    K = 512
+    members = [(synth.Q4_K, 256), (synth.Q4_K, 128)]
+    g, datas, hs = _register(members, K, seed=31, flags=0)
+    hn = mq.mq_register_weight(members[1][0], dev(datas[1]), members[1][1], K, flags=mq.MQ_REG_NO_CACHE)
+    x = synth.activations(g, 160, K)
+    refs = [orc.decode_matrix(qt, d, N, K) for (qt, N), d in zip(members, datas)]
+    old = mq.mq_get_m_gate()
+    try:
+        mq.mq_set_m_gate(100)
+        for M, group, want in ((16, hs, mq.MQ_TRACE_GEMM_FUSED), (99, hs, mq.MQ_TRACE_GEMM_FUSED),
+                               (100, hs, mq.MQ_TRACE_GEMM_CACHED), (160, hs, mq.MQ_TRACE_GEMM_CACHED),
+                               (160, [hs[0], hn], mq.MQ_TRACE_GEMM_FUSED)):
+            ys = [torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") for _, N in members]
+            mq.mq_trace_enable(True)
+            mq.mq_gemm_auto_grouped(dev(x[:M]), group, ys, M)
+            mq.mq_stream_status()
+            kinds = {r["kind"] for r in mq.mq_trace_records()}
+            mq.mq_trace_enable(False)
+            assert kinds == {want}, f"M={M}: trace kinds {kinds}"
+            for i, (y, W) in enumerate(zip(ys, refs)):
+                assert_gemm_close(y.cpu().numpy(), orc.gemm_f64(x[:M].view(np.uint16), W), f"auto M={M} member {i}")
+    finally:
+        mq.mq_set_m_gate(old)
+    for h in hs + [hn]:
+        h.release()
