@@ -5,7 +5,8 @@
 
 Cases: cached (mq_gemm), fused (mq_gemm_fused), decode (mq_dequantize),
 e4m3 (mq_gemm_e4m3 on activations quantized once before), quant
-(mq_quantize_e4m3 of the M x K activations).
+(mq_quantize_e4m3 of the M x K activations).  --group G (cached, fused): G
+weights of the shape in one mq_gemm_grouped / mq_gemm_fused_grouped call.
 Inputs are the seeded synthetic blocks of the given shape.  Prints the
 device time of each call from the library's trace events (not valid under a
 profiler, which serialises and replays kernels).
@@ -31,6 +32,7 @@ def main(argv=None):
     ap.add_argument("--M", type=int, default=32)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--group", type=int, default=1)
     args = ap.parse_args(argv)
 
     qtype = TYPES[args.type]
@@ -51,6 +53,15 @@ def main(argv=None):
             fn = lambda: mq.mq_quantize_e4m3(x, x8, sx)  # noqa: E731
         else:
             fn = lambda: mq.mq_gemm_e4m3(x8, sx, h, y, args.M)  # noqa: E731
+    elif args.group > 1:
+        flags = mq.MQ_REG_NO_CACHE if args.case == "fused" else 0
+        qs = [q] + [torch.from_numpy(synth.weight_bytes(g, qtype, args.N, args.K)).cuda()
+                    for _ in range(args.group - 1)]
+        hs = [mq.mq_register_weight(qtype, qi, args.N, args.K, flags=flags) for qi in qs]
+        x = torch.from_numpy(synth.activations(g, args.M, args.K)).cuda()
+        ys = [torch.empty((args.M, args.N), dtype=torch.float32, device="cuda") for _ in hs]
+        call = mq.mq_gemm_fused_grouped if args.case == "fused" else mq.mq_gemm_grouped
+        fn = lambda: call(x, hs, ys, args.M)  # noqa: E731
     else:
         flags = mq.MQ_REG_NO_CACHE if args.case == "fused" else 0
         h = mq.mq_register_weight(qtype, q, args.N, args.K, flags=flags)
@@ -65,7 +76,7 @@ def main(argv=None):
     torch.cuda.synchronize()
     mq.mq_stream_status()
     for r in mq.mq_trace_records():
-        print(f"{args.case} {args.type} M={args.M} N={args.N} K={args.K}: "
+        print(f"{args.case} {args.type} M={args.M} N={args.N}x{args.group} K={args.K}: "
               f"{r['ms_main'] * 1e3:.1f} us (+ reduce {r['ms_aux'] * 1e3:.1f} us)")
     mq.mq_trace_enable(False)
 
