@@ -10,18 +10,28 @@ where a tile grid's last wave underfills the GPU.  Weights q/k/v/o/gate/up are
 Q4_K, down is Q6_K, all seeded synthetic bytes with the model's shapes; they
 are registered (decoded once into the f16 cache) before timing.
 
-Printed: one JSON line (rank 0) with the contract keys plus
-  roofline      the cached GEMM kernel against the measured dense peak, its
-                per-launch duration read from CUDA events that the library
-                records on the launching stream during the timed steps;
-  cpu_baseline  the CPU oracle (f64) on a bounded sample of the same layer;
+Printed: one JSON line with the contract keys plus
+  roofline      the cached GEMM kernel against the measured dense peak: its
+                time per step is its share of the kernel time in a traced
+                pass (library trace events around every launch) times the
+                untraced step time; the f16 matmul peak is re-measured in
+                the same run;
+  cpu_baseline  the CPU oracle (f64) on a bounded sample of the same layer,
+                on all host cores and on one core, plus the oracle's
+                decoders per format and its GEMM time per configuration;
   e2e           the same metric with host buffers: pinned-host inputs copied
                 in and all outputs copied out inside the timed region;
-  decode        the one-time decoders (registration, cold) against HBM bandwidth;
+  decode        the registration decoders (mq_register_weight of the 7
+                weights back to back on a busy stream) against HBM bandwidth;
   decode_steady the decoders back to back on the 7B gate/down shapes and
                 weights of the other formats at the gate's shape (HBM GB/s);
   small_m       fused vs cached over the small-M sweep, back to back over
                 rotating weight copies (crossover, HBM GB/s);
+  c2_llama3.1-8b_layer  the Llama-3.1-8B layer at M = 512: cached (K-padded
+                caches and unpadded), fused and the M gate, per layer and
+                per GEMM;
+  c3_q8_0_pair  the Q8_0 pair: registration and steady decode, cached /
+                fused / M gate over M = 1 .. 1024 with its crossover;
   more_formats  Q4_0 / Q5_0 / Q5_1 / Q5_K at the 7B gate and down shapes:
                 fused and cached at M = 32 and 2048, same method;
   triangle      the 7B layer's seven GEMMs one call each through the cached
@@ -35,6 +45,8 @@ Printed: one JSON line (rank 0) with the contract keys plus
                 per step, seven e4m3 GEMMs; TFLOP/s, the e4m3 kernel against
                 the 8-bit dense peak, distance to the f16 result.
 
+One GPU per run: with --gpus N > 1 (or under torchrun with more than one
+rank) no rank touches a GPU and rank 0 prints a line that says so.
 --impl reference times the CPU oracle itself as the reference arm.
 """
 from __future__ import annotations
@@ -89,20 +101,9 @@ def layer_flops(weights, M):
     return sum(2.0 * M * w.N * w.K for w in weights)
 
 
-def max_over_ranks(x: float, dist=None, device="cpu") -> float:
-    """The largest x over all ranks (the job's time is its slowest rank's)."""
-    if dist is None:
-        return x
-    import torch
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def whole_job_tflops(world: int, flops_per_step: float, ms_per_step: float) -> float:
-    """Weak scaling: every rank runs its own step, the job does world steps
-    in the slowest rank's time."""
-    return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
+def layer_decode_bytes(weights):
+    """Algorithmic bytes of decoding the weights: blocks read + f16 written once."""
+    return sum(synth.nblocks(w.qtype, w.N, w.K) * synth.BLOCK[w.qtype][1] + 2 * w.N * w.K for w in weights)
 
 
 # ---------------------------------------------------------------- clocks
@@ -234,6 +235,10 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- our arm
 
+SINGLE_GPU_NOTE = ("single-GPU path: the library runs one GPU per process and nothing here launches it on "
+                   "more than one GPU (the path shards by tokens or weight rows with no exchange; see replicas)")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -241,49 +246,48 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget for cpu_baseline")
-    ap.add_argument("--no-extras", action="store_true", help="skip e2e, small-M sweep and cpu_baseline")
+    ap.add_argument("--no-extras", action="store_true", help="skip e2e, the extra workloads and cpu_baseline")
     ap.add_argument("--clocks-out", default=None)
+    ap.add_argument("--oracle-child", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_child:
+        return oracle_child(args.oracle_child)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
 
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.gpus > 1 or world > 1:
+        # One GPU per run: no rank touches a GPU; rank 0 says so.
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": None, "unit": "TFLOP/s", "n_gpus": max(args.gpus, world),
+                              "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                              "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+                              "config": {"workload": WORKLOAD, "M": M_TOKENS}, "skipped": SINGLE_GPU_NOTE}))
+        return 0
+
     import torch
     import quantized_weight_prefill_gguf_gb300 as mq
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
+    torch.cuda.set_device(0)
     P = peaks()
     weights, xs = synth.workload(WORKLOAD, seed=0)
-    # each rank processes its own batch of tokens (independent prefill u-batches)
-    if rank > 0:
-        g = synth.rng(1000 + rank)
-        xs = {k: synth.activations(g, M_TOKENS, k) for k in xs}
 
     stream = torch.cuda.current_stream()
     qdev = [torch.from_numpy(w.data).cuda() for w in weights]
     torch.cuda.synchronize()
 
     # registration = one-time decode into the f16 caches, traced per weight
+    # (the process's first decode launches: cold, see registration_decode)
     mq.mq_trace_enable(True)
     handles = [mq.mq_register_weight(w.qtype, q, w.N, w.K) for w, q in zip(weights, qdev)]
     torch.cuda.synchronize()
     dec = [r for r in mq.mq_trace_records() if r["kind"] == mq.MQ_TRACE_DECODE]
     mq.mq_trace_enable(False)
-    decode_bytes = sum(synth.nblocks(w.qtype, w.N, w.K) * synth.BLOCK[w.qtype][1] + 2 * w.N * w.K for w in weights)
-    decode_ms = sum(r["ms_main"] for r in dec)
+    decode_bytes = layer_decode_bytes(weights)
+    decode_cold_ms = sum(r["ms_main"] for r in dec)
 
     xdev = {k: torch.from_numpy(v).cuda() for k, v in xs.items()}
     ys = [torch.empty((M_TOKENS, w.N), dtype=torch.float32, device="cuda") for w in weights]
@@ -298,28 +302,26 @@ def main():
     mq.mq_stream_status()
 
     # ---- timed region
-    clocks = ClockSampler(local_rank, args.clocks_out)
+    clocks = ClockSampler(0, args.clocks_out)
     clocks.start()
     time.sleep(0.3)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = mq.mq_launch_count()
-    barrier()
     torch.cuda.synchronize()
     ev0.record(stream)
     for _ in range(args.steps):
         step(xdev)
     ev1.record(stream)
     torch.cuda.synchronize()
-    barrier()
     launches = mq.mq_launch_count() - launches0
     clk = clocks.stop()
     mq.mq_stream_status()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dist, "cuda")
+    ms = ev0.elapsed_time(ev1) / args.steps
 
-    # Per-kernel durations for the roofline: a separate pass with the
-    # library's trace events (events recorded between two launches end the
+    # Kernel shares for the roofline: a separate pass with the library's
+    # trace events around every launch (events between two launches end the
     # overlap that programmatic dependent launch gives, so the timed steps
-    # above run without them).
+    # above run without them; only the shares are taken from this pass).
     trace_steps = min(args.steps, 200)
     mq.mq_trace_enable(True)
     for _ in range(trace_steps):
@@ -328,12 +330,12 @@ def main():
     mq.mq_trace_enable(False)
 
     flops_step = layer_flops(weights, M_TOKENS)
-    value = whole_job_tflops(world, flops_step, ms)
+    value = flops_step / (ms * 1e-3) / 1e12
+    f16_peak = f16_matmul_peak(torch)
 
-    # ---- roofline of the dominant kernel: the cached GEMM (k_gemm_cached)
+    # ---- roofline of the dominant kernel: the cached GEMM (k_gemm_cached*)
     recs = mq.mq_trace_records()
     gem = [r for r in recs if r["kind"] == mq.MQ_TRACE_GEMM_CACHED]
-    g_flops = sum(2.0 * r["M"] * r["N"] * r["K"] for r in gem)
     g_ms = sum(r["ms_main"] for r in gem)
     red_ms = sum(r["ms_aux"] for r in gem)
     per_gemm = []
@@ -346,10 +348,15 @@ def main():
             t_aux = statistics.median(r["ms_aux"] for r in rs)
             per_gemm.append({"name": "|".join(grp), "N": n_tot, "K": K_,
                              "type": "/".join(sorted({synth.TYPE_NAME[w.qtype] for w in ws_})),
-                             "gemm_us": t_main * 1e3, "reduce_us": t_aux * 1e3,
-                             "tflops": 2.0 * M_TOKENS * n_tot * K_ / ((t_main + t_aux) * 1e-3) / 1e12})
-    n_launch = max(1, len(gem))
-    achieved = (g_flops / n_launch) / ((g_ms / n_launch) * 1e-3) / 1e12 if g_ms > 0 else None
+                             "gemm_us_traced": t_main * 1e3, "reduce_us_traced": t_aux * 1e3})
+    # The GEMM kernel's time per step = its share of the traced kernel time
+    # (GEMM + split-K reduce) x the untraced step time; all the step's FLOPs
+    # are the GEMM kernel's (the reduce only adds partial planes).
+    share = g_ms / (g_ms + red_ms) if g_ms > 0 else None
+    kern_ms = share * ms if share else None
+    if kern_ms is not None:
+        assert kern_ms <= ms * (1 + 1e-9), "kernel time per step exceeds the step"
+    achieved = flops_step / (kern_ms * 1e-3) / 1e12 if kern_ms else None
     traffic = None
     tp = os.path.join(ROOT, "profiles", "k_gemm_cached.qwen2.5-7b_layer.traffic.json")
     if os.path.exists(tp):
@@ -358,16 +365,23 @@ def main():
         # the counters only describe the kernel source they were taken from
         if rec.get("kernel_source_sha256") == cached_kernel_source_hash():
             traffic = rec.get("k_gemm_cached_bytes_per_launch")
+    n_launch = max(1, len(gem) // max(1, trace_steps))
     roofline = {"bound": "tensor", "achieved": achieved, "peak": P["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": (achieved / P["bf16_tflops"]) if achieved else None, "traffic": traffic,
-                "kernel": "k_gemm_cached (tcgen05 f16 GEMM on the f16 cache)",
-                "peak_kind": f"dense bf16 burst ({P['source']}); f16 nominal rate equals bf16",
+                "kernel": "k_gemm_cached_2sm / k_gemm_cached (tcgen05 f16 GEMM on the f16 cache)",
+                "peak_kind": f"dense bf16 burst ({P['source']}); the f16 nominal rate equals bf16",
+                "peak_f16_same_run": f16_peak,
+                "frac_of_f16_same_run": (achieved / f16_peak) if achieved and f16_peak else None,
                 "frac_of_sustained": (achieved / P["bf16_tflops_sustained"]) if achieved else None,
-                "launches_traced": len(gem), "traced_steps": trace_steps,
-                "reduce_ms_per_step": red_ms / trace_steps}
+                "step_frac": value / P["bf16_tflops"],
+                "kernel_share_of_step": share, "kernel_ms_per_step": kern_ms,
+                "launches_per_step": n_launch,
+                "method": "achieved = the step's FLOPs / (GEMM kernel share of the traced kernel time x the "
+                          "untraced ms_per_step); traffic = DRAM bytes per launch from one ncu capture",
+                "traced_steps": trace_steps, "reduce_share_of_step": (1 - share) if share else None}
 
     out = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M_TOKENS, "gemms": [w.name for w in weights],
@@ -375,39 +389,33 @@ def main():
                    "gflop_per_step": flops_step / 1e9,
                    "path": "mq_gemm_grouped (q|k|v, gate|up) + mq_gemm_auto -> cached (o, down)",
                    "l2": "inputs larger than L2: 466 MB of f16 weight caches per step vs 126 MB L2",
-                   "parallelism": f"replicas x{world} (independent token batches)"},
-        "tok_per_s_per_layer": world * M_TOKENS / (ms * 1e-3),
-        "tok_per_s_28_layer_gemms_only": world * M_TOKENS / (28 * ms * 1e-3),
-        "frac_of_peak": value / world / P["bf16_tflops"],
+                   "parallelism": "one GPU"},
+        "tok_per_s_per_layer": M_TOKENS / (ms * 1e-3),
+        "tok_per_s_28_layer_gemms_only": M_TOKENS / (28 * ms * 1e-3),
+        "frac_of_peak": value / P["bf16_tflops"],
         "roofline": roofline,
         "per_gemm": per_gemm,
         "gpu_launches": launches,
         "clocks": clk,
-        "decode": {"bytes": decode_bytes, "ms": decode_ms,
-                   "gbs": decode_bytes / (decode_ms * 1e-3) / 1e9 if decode_ms else None,
-                   "frac_hbm": (decode_bytes / (decode_ms * 1e-3) / 1e9) / P["hbm_gbs"] if decode_ms else None,
-                   "note": "one-time registration decode of the 7 weights (blocks read + f16 written), cold"},
     }
+    out["decode"] = registration_decode(mq, torch, stream, weights, qdev, P)
+    out["decode"]["cold_ms"] = decode_cold_ms
+    out["decode"]["cold_gbs"] = decode_bytes / (decode_cold_ms * 1e-3) / 1e9 if decode_cold_ms else None
 
     if not args.no_extras:
-        out["e2e"] = e2e_run(mq, torch, weights, handles, xs, ys, stream, min(args.steps, 50), flops_step, dist)
+        out["e2e"] = e2e_run(mq, torch, weights, handles, xs, ys, stream, min(args.steps, 50), flops_step)
         out["small_m"] = small_m_sweep(mq, torch, stream, P)
         out["decode_steady"] = decode_steady(mq, torch, stream, P)
+        out["c2_llama3.1-8b_layer"] = llama_layer(mq, torch, stream, P)
+        out["c3_q8_0_pair"] = q8_pair(mq, torch, stream, P)
         out["more_formats"] = more_formats(mq, torch, stream, P)
         out["triangle"] = triangle(mq, torch, stream, weights, handles, qdev, xdev)
         out["row_pad"] = row_pad(mq, torch, stream)
         out["e4m3"] = e4m3_layer(mq, torch, stream, weights, qdev, xdev, ys, P, min(args.steps, 400), flops_step)
-    if rank == 0 and world == 1 and not args.no_extras:
-        tf, tokens, secs, dsec, threads = oracle_cpu_run(weights, xs, args.cpu_seconds)
-        out["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                               "sample": f"{tokens} of {M_TOKENS} tokens through all 7 GEMMs (f64, {secs:.1f} s); "
-                                         f"oracle decode of the 7 weights took {dsec:.1f} s before"}
+        out["cpu_baseline"] = cpu_baseline(weights, xs, args.cpu_seconds)
     for h in handles:
         h.release()
-    if rank == 0:
-        print(json.dumps(out))
-    if dist is not None:
-        dist.destroy_process_group()
+    print(json.dumps(out))
     return 0
 
 
@@ -428,7 +436,7 @@ def layer_step(mq, weights, handles, ys, xmap, M, stream):
             mq.mq_gemm_grouped(x, [handles[i] for i in idx], [ys[i] for i in idx], M, stream)
 
 
-def e2e_run(mq, torch, weights, handles, xs, ys, stream, steps, flops_step, dist):
+def e2e_run(mq, torch, weights, handles, xs, ys, stream, steps, flops_step):
     """The step through the public API with host buffers: every step copies
     its activations in from pinned host memory and all seven outputs back to
     pinned host memory, inside the timed region.  Copies run on their own
@@ -471,8 +479,6 @@ def e2e_run(mq, torch, weights, handles, xs, ys, stream, steps, flops_step, dist
         step(t)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
     e0.record(stream)
     s_in.wait_event(e0)
     s_out.wait_event(e0)
@@ -482,9 +488,8 @@ def e2e_run(mq, torch, weights, handles, xs, ys, stream, steps, flops_step, dist
     stream.wait_stream(s_out)
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1) / steps, dist, "cuda")
-    world = dist.get_world_size() if dist is not None else 1
-    return {"value": whole_job_tflops(world, flops_step, ms), "unit": "TFLOP/s", "ms_per_step": ms,
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": flops_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "copies": "pinned host <-> device on two copy streams, double-buffered device X and Y"}
 
@@ -507,37 +512,53 @@ def _rotating_time_us(torch, fns, stream, reps=5):
     return statistics.median(ts)
 
 
-def _fused_vs_cached(mq, torch, stream, P, w, x_all, ms):
+def _paths_rotating(mq, torch, stream, P, w, x_all, ms, paths=("fused", "cached")):
     """Rows {name, M, copies, <path>_us/_tflops/_gbs/_frac_hbm} for weight w
-    at each M: per-call time of calls issued back to back over R registered
-    copies of the weight, R chosen so the weights touched (raw blocks for
-    fused, f16 caches for cached) exceed 400 MB, three times the L2: every
-    call streams its weight from HBM, as in a layer stack, and the launch gap
-    between calls is included."""
+    at each M and each path of `paths` ("fused": mq_gemm_fused, "cached":
+    mq_gemm, "cached_nokpad": mq_gemm on copies registered with
+    MQ_REG_NO_KPAD, "auto": mq_gemm_auto): per-call time of calls issued back
+    to back over R registered copies of the weight, R chosen so the weights
+    touched (raw blocks for fused, f16 caches for cached) exceed 400 MB, three
+    times the L2: every call streams its weight from HBM, as in a layer stack,
+    and the launch gap between calls is included.  "auto" is charged the
+    bytes of the path the M gate picks."""
     raw_bytes = synth.nblocks(w.qtype, w.N, w.K) * synth.BLOCK[w.qtype][1]
     R = max(3, -(-(400 << 20) // raw_bytes))
     qs = [torch.from_numpy(w.data).cuda() for _ in range(R)]
     hs = [mq.mq_register_weight(w.qtype, q, w.N, w.K) for q in qs]
+    hs_nokpad = ([mq.mq_register_weight(w.qtype, q, w.N, w.K, flags=mq.MQ_REG_NO_KPAD) for q in qs]
+                 if "cached_nokpad" in paths else [])
+    fns = {"fused": (mq.mq_gemm_fused, hs), "cached": (mq.mq_gemm, hs), "cached_nokpad": (mq.mq_gemm, hs_nokpad),
+           "auto": (mq.mq_gemm_auto, hs)}
+    gate = mq.mq_get_m_gate()
     rows = []
     for M in ms:
         x = x_all[:M].contiguous()
         y = torch.empty((M, w.N), dtype=torch.float32, device="cuda")
         row = {"name": w.name, "M": M, "copies": R}
-        for path, fn in (("fused", mq.mq_gemm_fused), ("cached", mq.mq_gemm)):
-            calls = [functools.partial(fn, x, h, y, M, stream) for h in hs]
+        for path in paths:
+            fn, hh = fns[path]
+            calls = [functools.partial(fn, x, h, y, M, stream) for h in hh]
             t_us = _rotating_time_us(torch, calls, stream)
-            wbytes = raw_bytes if path == "fused" else 2 * w.N * w.K
+            fused_bytes = path == "fused" or (path == "auto" and M < gate)
+            wbytes = raw_bytes if fused_bytes else 2 * w.N * w.K
             byts = wbytes + 2 * M * w.K + 4 * M * w.N
             row[path + "_us"] = t_us
             row[path + "_tflops"] = 2.0 * M * w.N * w.K / (t_us * 1e-6) / 1e12
             row[path + "_gbs"] = byts / (t_us * 1e-6) / 1e9
             row[path + "_frac_hbm"] = row[path + "_gbs"] / P["hbm_gbs"]
+        if "auto" in paths:
+            row["auto_took"] = "fused" if M < gate else "cached"
         rows.append(row)
     mq.mq_stream_status()
-    for h in hs:
+    for h in hs + hs_nokpad:
         h.release()
     del qs
     return rows
+
+
+def _fused_vs_cached(mq, torch, stream, P, w, x_all, ms):
+    return _paths_rotating(mq, torch, stream, P, w, x_all, ms, ("fused", "cached"))
 
 
 def small_m_sweep(mq, torch, stream, P):
@@ -690,7 +711,7 @@ def e4m3_layer(mq, torch, stream, weights, qdev, xdev, ys_f16, P, steps, flops_s
     achieved = sum(kern_flops) / (sum(kern_ms) * 1e-3) / 1e12 if recs else None
     peak8 = 2.0 * P["bf16_tflops"]
     gi = idx["gate"]
-    dist = float(torch.linalg.norm(ys[gi] - ys_f16[gi]) / torch.linalg.norm(ys_f16[gi]))
+    rel = float(torch.linalg.norm(ys[gi] - ys_f16[gi]) / torch.linalg.norm(ys_f16[gi]))
     mq.mq_stream_status()
     for h in hs:
         h.release()
@@ -699,7 +720,7 @@ def e4m3_layer(mq, torch, stream, weights, qdev, xdev, ys_f16, P, steps, flops_s
             "kernel": {"name": "k_gemm_e4m3", "achieved_tflops": achieved, "peak_tflops": peak8,
                        "peak_note": "8-bit dense = 2 x the measured bf16 burst peak (the nominal fp8:bf16 ratio)",
                        "frac": achieved / peak8 if achieved else None},
-            "rel_distance_to_f16_gate": dist,
+            "rel_distance_to_f16_gate": rel,
             "note": "separate numeric contract: e4m3 operands with per-row / per-token f32 scales"}
 
 
@@ -750,6 +771,277 @@ def decode_steady(mq, torch, stream, P):
         del qs, dst
     mq.mq_stream_status()
     return out
+
+
+def f16_matmul_peak(torch, n=8192, reps=10):
+    """Dense f16 tensor-core rate measured in this run: torch.matmul (a
+    library GEMM, used only as the roofline's denominator) on n x n x n f16
+    operands, best of `reps` single calls after warm-up (burst clocks)."""
+    a = torch.randn(n, n, device="cuda", dtype=torch.float16)
+    b = torch.randn(n, n, device="cuda", dtype=torch.float16)
+    for _ in range(3):
+        torch.matmul(a, b)
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1)
+        best = t if best is None else min(best, t)
+    del a, b
+    return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+
+
+def registration_decode(mq, torch, stream, weights, qdev, P):
+    """mq_register_weight of the given weights as one sequence, the product's
+    decode entry point: each call allocates the f16 cache and enqueues the
+    decoder.  Timed on the device with CUDA events around the whole
+    sequence while a sleep kernel keeps the stream busy until the host has
+    issued every call, so neither host launch latency nor an idle GPU enters
+    the window (a single event-timed call on an idle GPU includes the host's
+    launch latency).  A first, untimed pass loads the decode kernels.  Best
+    of three, with no events between the calls (an event between two
+    launches ends their programmatic overlap); `kernel_ms` sums the decode
+    kernels' own durations from the library's trace events in a separate
+    pass."""
+    nbytes = layer_decode_bytes(weights)
+
+    def register_all():
+        return [mq.mq_register_weight(w.qtype, q, w.N, w.K, stream=stream) for w, q in zip(weights, qdev)]
+
+    t0 = time.perf_counter()
+    hs = register_all()
+    torch.cuda.synchronize()
+    host_s = time.perf_counter() - t0
+    for h in hs:
+        h.release()
+    busy_s = max(0.002, 4.0 * host_s)
+    best = None
+    for _ in range(3):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(busy_s * 2.5e9))
+        e0.record(stream)
+        t0 = time.perf_counter()
+        hs = register_all()
+        issue_s = time.perf_counter() - t0
+        e1.record(stream)
+        torch.cuda.synchronize()
+        seq_ms = e0.elapsed_time(e1)
+        for h in hs:
+            h.release()
+        if best is None or seq_ms < best["ms"]:
+            best = {"ms": seq_ms, "issue_ms": issue_s * 1e3, "busy_ms": busy_s * 1e3}
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(busy_s * 2.5e9))
+    mq.mq_trace_enable(True)
+    hs = register_all()
+    torch.cuda.synchronize()
+    kern_ms = sum(r["ms_main"] for r in mq.mq_trace_records() if r["kind"] == mq.MQ_TRACE_DECODE)
+    mq.mq_trace_enable(False)
+    for h in hs:
+        h.release()
+    gbs = nbytes / (best["ms"] * 1e-3) / 1e9
+    best.update({"bytes": nbytes, "gbs": gbs, "frac_hbm": gbs / P["hbm_gbs"], "kernel_ms_traced": kern_ms,
+                 "kernel_gbs_traced": nbytes / (kern_ms * 1e-3) / 1e9 if kern_ms else None,
+                 "stream_stayed_busy": best["issue_ms"] < best["busy_ms"],
+                 "weights": len(weights),
+                 "note": "mq_register_weight of every weight back to back (blocks read + f16 written once), "
+                         "device-timed on a busy stream; kernel_*_traced: events around each decode (no "
+                         "launch overlap); cold_* = the process's first registration, event-timed per call on "
+                         "an idle GPU (kernel loading and host launch latency included)"})
+    return best
+
+
+LLAMA_M = 512
+
+
+def llama_layer(mq, torch, stream, P):
+    """Config c2: the Llama-3.1-8B-shaped layer (all Q4_K; K = 4096 and
+    14336, so the f16 caches are K-padded by one 128-byte line) at M = 512.
+    Per layer (the layer's four launch groups back to back, rotating over
+    R copies of the layer: > 400 MB of raw blocks touched): cached (padded
+    caches), cached without the pad (MQ_REG_NO_KPAD), fused (raw blocks)
+    and the M gate (auto).  Per GEMM shape: the same paths on single
+    weights (_paths_rotating)."""
+    clocks = ClockSampler(0)
+    clocks.start()
+    weights, xs = synth.workload("llama3.1-8b_layer", seed=0)
+    M = LLAMA_M
+    xdev = {K: torch.from_numpy(x[:M]).cuda() for K, x in xs.items()}
+    raw = sum(w.data.size for w in weights)
+    R = max(2, -(-(400 << 20) // raw))
+    copies = []
+    for _ in range(R):
+        q = [torch.from_numpy(w.data).cuda() for w in weights]
+        copies.append({"q": q,
+                       "cached": [mq.mq_register_weight(w.qtype, qq, w.N, w.K) for w, qq in zip(weights, q)],
+                       "cached_nokpad": [mq.mq_register_weight(w.qtype, qq, w.N, w.K, flags=mq.MQ_REG_NO_KPAD)
+                                         for w, qq in zip(weights, q)],
+                       "fused": [mq.mq_register_weight(w.qtype, qq, w.N, w.K, flags=mq.MQ_REG_NO_CACHE)
+                                 for w, qq in zip(weights, q)]})
+    ys = [torch.empty((M, w.N), dtype=torch.float32, device="cuda") for w in weights]
+    by = {w.name: i for i, w in enumerate(weights)}
+    groups = [[by[n] for n in grp] for grp in LAUNCH_GROUPS]
+    single = {"cached": mq.mq_gemm, "cached_nokpad": mq.mq_gemm, "fused": mq.mq_gemm_fused, "auto": mq.mq_gemm_auto}
+    grouped = {"cached": mq.mq_gemm_grouped, "cached_nokpad": mq.mq_gemm_grouped,
+               "fused": mq.mq_gemm_fused_grouped, "auto": mq.mq_gemm_auto_grouped}
+
+    def layer_fn(c, mode):
+        hs = c["cached" if mode == "auto" else mode]
+
+        def run():
+            for idx in groups:
+                x = xdev[weights[idx[0]].K]
+                if len(idx) == 1:
+                    single[mode](x, hs[idx[0]], ys[idx[0]], M, stream)
+                else:
+                    grouped[mode](x, [hs[i] for i in idx], [ys[i] for i in idx], M, stream)
+        return run
+
+    flops = layer_flops(weights, M)
+    layer = {}
+    for mode in ("cached", "cached_nokpad", "fused", "auto"):
+        t_us = _rotating_time_us(torch, [layer_fn(c, mode) for c in copies], stream)
+        layer[mode + "_us"] = t_us
+        layer[mode + "_tflops"] = flops / (t_us * 1e-6) / 1e12
+    mq.mq_stream_status()
+    ldk = copies[0]["cached"][0].info()[2]
+    for c in copies:
+        for h in c["cached"] + c["cached_nokpad"] + c["fused"]:
+            h.release()
+    del copies
+    per_gemm = []
+    for name in ("q", "k", "gate", "down"):
+        w = weights[by[name]]
+        per_gemm += _paths_rotating(mq, torch, stream, P, w, xdev[w.K], [M],
+                                    ("cached", "cached_nokpad", "fused", "auto"))
+    clk = clocks.stop()
+    return {"M": M, "gflop_per_layer": flops / 1e9, "ldk_padded": ldk, "layer": layer, "layer_copies": R,
+            "per_gemm": per_gemm, "gate_in_use": mq.mq_get_m_gate(), "clocks": clk,
+            "method": "layer = four launches (q|k|v and gate|up grouped, o, down) back to back over R layer "
+                      "copies; per GEMM as small_m (rotating copies, > 400 MB touched)"}
+
+
+def q8_pair(mq, torch, stream, P):
+    """Config c3: Q8_0 weights 3584 x 18944 and 18944 x 3584 (34-byte blocks,
+    2-byte aligned; K = 18944 and 3584 are not multiples of 1024, so the
+    caches are not padded).  Decode through mq_register_weight (busy-stream
+    sequence) and mq_dequantize back to back; GEMMs through the cached path,
+    the fused path and the M gate at M in {1, 8, 32, 128, 256, 512, 1024}
+    (M = 128 and 1024 are the configuration's own), rotating copies."""
+    clocks = ClockSampler(0)
+    clocks.start()
+    weights, xs = synth.workload("q8_0_pair", seed=0)
+    qdev = [torch.from_numpy(w.data).cuda() for w in weights]
+    reg = registration_decode(mq, torch, stream, weights, qdev, P)
+    steady = {}
+    for w, q in zip(weights, qdev):
+        qs = [q] + [q.clone() for _ in range(2)]
+        dst = torch.empty((w.N, w.K), dtype=torch.float16, device="cuda")
+        calls = [functools.partial(mq.mq_dequantize, w.qtype, qq, w.N, w.K, dst, None, stream) for qq in qs] * 4
+        t_us = _rotating_time_us(torch, calls, stream)
+        byts = layer_decode_bytes([w])
+        steady[w.name] = {"N": w.N, "K": w.K, "us": t_us, "gbs": byts / (t_us * 1e-6) / 1e9,
+                          "frac_hbm": byts / (t_us * 1e-6) / 1e9 / P["hbm_gbs"]}
+        del qs, dst
+    rows = []
+    for w in weights:
+        x_all = torch.from_numpy(xs[w.K]).cuda()
+        rows += _paths_rotating(mq, torch, stream, P, w, x_all, [1, 8, 32, 128, 256, 512, 1024],
+                                ("fused", "cached", "auto"))
+    cross = {}
+    for w in weights:
+        ms_ = [r["M"] for r in rows if r["name"] == w.name and r["cached_us"] <= r["fused_us"]]
+        cross[w.name] = min(ms_) if ms_ else None
+    flops_pair = {M: sum(2.0 * M * w.N * w.K for w in weights) for M in (128, 1024)}
+    headline = {}
+    for M in (128, 1024):
+        sel = [r for r in rows if r["M"] == M]
+        headline[f"M{M}"] = {p + "_tflops_pair": flops_pair[M] / (sum(r[p + "_us"] for r in sel) * 1e-6) / 1e12
+                             for p in ("fused", "cached", "auto")}
+    clk = clocks.stop()
+    return {"decode_registration": reg, "decode_steady": steady, "rows": rows, "headline": headline,
+            "cached_wins_from_M": cross, "gate_in_use": mq.mq_get_m_gate(), "clocks": clk}
+
+
+def oracle_child(tokens: int) -> int:
+    """Child process of cpu_baseline: time the oracle's f64 GEMM over the 7B
+    layer for `tokens` tokens with the OpenMP thread count this process was
+    started with (OMP_NUM_THREADS); print one JSON line."""
+    import oracle
+    orc = oracle.load()
+    weights, xs = synth.workload(WORKLOAD, seed=0)
+    W16 = [orc.decode_matrix(w.qtype, w.data, w.N, w.K) for w in weights]
+    t0 = time.perf_counter()
+    for w, W in zip(weights, W16):
+        orc.gemm_f64(xs[w.K][:tokens].view(np.uint16), W)
+    secs = time.perf_counter() - t0
+    print(json.dumps({"tokens": tokens, "secs": secs, "threads": orc.num_threads(),
+                      "tflops": layer_flops(weights, tokens) / secs / 1e12}))
+    return 0
+
+
+def cpu_baseline(weights, xs, budget_s):
+    """The oracle as it stands, timed on this host's cores: the 7B layer's f64
+    GEMM on a token sample sized to about budget_s seconds with every core
+    (the headline value), the same on one core (a child process with
+    OMP_NUM_THREADS=1, a smaller sample), the oracle's decoders per format
+    (best of 3, GB/s of blocks read + f16 written) and its GEMM time per
+    configuration, extrapolated linearly in M from a token sample."""
+    import oracle
+    orc = oracle.load()
+    tf, tokens, secs, dsec, threads = oracle_cpu_run(weights, xs, budget_s)
+    res = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "sample": f"{tokens} of {M_TOKENS} tokens through all 7 GEMMs of the 7B layer (f64, {secs:.1f} s) "
+                     f"on all {threads} threads; the oracle's decode of the 7 weights took {dsec:.1f} s before",
+           "cores_all": threads}
+    per_tok_1 = secs / tokens * threads   # rough single-core cost per token, sizes the child's sample
+    t1 = int(max(1, min(M_TOKENS, 8.0 / max(per_tok_1, 1e-9))))
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", str(t1)], env=env,
+                           capture_output=True, text=True, timeout=300)
+        child = json.loads(r.stdout.strip().splitlines()[-1])
+        res["value_1core"] = child["tflops"]
+        res["sample_1core"] = f"{child['tokens']} tokens, {child['secs']:.1f} s, {child['threads']} thread"
+    except (subprocess.SubprocessError, ValueError, IndexError, KeyError) as e:
+        res["value_1core"] = None
+        res["sample_1core"] = f"failed: {e}"
+    g = synth.rng(5)
+    dec = {}
+    for qt, N, K in ((synth.Q4_K, 18944, 3584), (synth.Q6_K, 3584, 18944), (synth.Q8_0, 18944, 3584)):
+        data = synth.weight_bytes(g, qt, N, K)
+        best = None
+        for _ in range(3):
+            t0 = time.perf_counter()
+            orc.decode_matrix(qt, data, N, K)
+            t = time.perf_counter() - t0
+            best = t if best is None else min(best, t)
+        dec[synth.TYPE_NAME[qt]] = {"N": N, "K": K, "s": best,
+                                    "gbs": layer_decode_bytes([synth.Weight("w", qt, N, K, data)]) / best / 1e9}
+    res["decode_gbs"] = dec
+    per_cfg = {}
+    for name in ("q4k_896", "qwen2.5-7b_layer", "llama3.1-8b_layer", "q8_0_pair"):
+        ws, xx = synth.workload(name, seed=0)
+        W16 = [orc.decode_matrix(w.qtype, w.data, w.N, w.K) for w in ws]
+        Ms = synth.WORKLOADS[name][1]
+        t_tok = 16
+        t0 = time.perf_counter()
+        for w, W in zip(ws, W16):
+            orc.gemm_f64(xx[w.K][:t_tok].view(np.uint16), W)
+        per_tok = (time.perf_counter() - t0) / t_tok
+        per_cfg[name] = {f"M{M}_s_est": per_tok * M for M in Ms}
+        per_cfg[name]["sample_tokens"] = t_tok
+    res["gemm_s_per_config"] = per_cfg
+    res["gemm_s_note"] = ("f64 GEMM of every weight of the configuration, all threads; seconds for the full M "
+                          "estimated from a 16-token sample (the GEMM's cost is linear in M)")
+    return res
 
 
 if __name__ == "__main__":

@@ -374,27 +374,46 @@ int mq_debug_schedule(int64_t M, int64_t N, int64_t K, int sms, int path, int pa
                       int32_t *units, int64_t cap, int64_t *count);
 
 /*
- * mq_gemm_noalloc -- the cached GEMM (same result as mq_gemm, same
- * arguments) for callers that cannot allocate device memory: code that runs
- * while a stream is captured into a CUDA graph in global capture mode (where
- * cudaMalloc is refused), engines whose own pool owns the device's memory and
- * forbids other allocations, and latency-critical paths that must not risk
- * the implicit synchronization an allocation or a free can cause.  mq_gemm
- * may grow its split-K scratch with cudaMalloc on first use; this entry point
- * never calls cudaMalloc, cudaFree or any allocating routine.  No page
- * describes it: it is this library's own addition.
+ * mq_debug_cvt_f16 -- test hook for the decoders' last step, the f32 -> f16
+ * rounding (round to nearest even, subnormals kept, sign of zero kept:
+ * "05 · 8p — Persistent f16 weight cache + fused dequant-in-GEMM",
+ * section 3.3 Pitfalls, the fused and cached decodes must round through the
+ * same path).  Writes to out[i] (device, uint16, count elements) the f16
+ * bits that the decoders' own packed conversion gives for the binary32 bit
+ * pattern first + i.  first and count must be even and first + count <=
+ * 2^32; out 4-byte aligned.  Stream-ordered.  Errors: MQ_ERR_INVALID,
+ * MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_CUDA.
+ */
+int mq_debug_cvt_f16(uint32_t first, int64_t count, void *out, void *stream);
+
+/*
+ * mq_gemm_noalloc -- the cached GEMM, same arguments as mq_gemm, for
+ * callers that cannot allocate device memory: engines and serving runtimes
+ * whose own pool reserves the device's memory up front and forbids any
+ * other allocation, and latency-critical paths that must not risk the
+ * implicit device synchronization a cudaMalloc or cudaFree can cause.
+ * mq_gemm may grow its split-K scratch with cudaMalloc on first use; this
+ * entry point never calls cudaMalloc, cudaFree or any allocating routine.
+ * No page describes it: the pages have no counterpart, it is this library's
+ * own addition.
+ *
+ * Result: within the GEMM tolerance of mq_gemm, not bit for bit.  It runs
+ * the single-CTA plan (no CTA pairs, no 2-SM MMAs) with its split-K tail
+ * bounded by the scratch below, so its summation order can differ; the
+ * tuning switches MQ_SPLITK, MQ_BN, MQ_PAIR and MQ_2SM do not apply to it.
  *
  * Its split-K scratch is one 16 MiB file-scope device array, which every GPU
  * that loads this library holds until the process exits.  A call whose split
  * plan needs more than 16 MiB fails with MQ_ERR_SHAPE and says so (at
  * M = 2048 that is the case for a 3584-row weight, for example).  The first
- * call on each device looks up the array's device address (with that device
- * current); make that first call before any stream capture.  All calls share
- * the array, so calls that overlap on the GPU (different streams, or graphs
- * replayed concurrently) race and must be serialized by the caller.  Every
- * call overwrites all the scratch it reads, so nothing needs clearing between
- * calls.  Device-side timeouts of these calls are reported by
- * mq_stream_status (whose own first call on a device does allocate).
+ * call on each device does a one-time set-up: it looks up the array's device
+ * address (with that device current).  Make that first call before any
+ * stream capture.  All calls share the array, so calls that overlap on the
+ * GPU (different streams, or graphs replayed concurrently) race and must be
+ * serialized by the caller.  Every call writes all the scratch it reads
+ * before reading it, so nothing needs clearing between calls.  Device-side
+ * timeouts of these calls are reported by mq_stream_status (whose own first
+ * call on a device does allocate).
  * Errors: as mq_gemm, plus MQ_ERR_SHAPE when the scratch is too small.
  */
 int mq_gemm_noalloc(const void *x, mq_handle w, float *y, int64_t M, void *stream);

@@ -29,7 +29,7 @@ EXPORTS = ("mq_register_weight", "mq_release_weight", "mq_weight_info", "mq_dequ
            "mq_stream_status", "mq_launch_count", "mq_error_string", "mq_last_error_detail", "mq_version",
            "mq_trace_enable", "mq_trace_count", "mq_trace_read", "mq_gemm_noalloc", "mq_gemm_grouped", "mq_gemm_fused_grouped", "mq_gemm_auto_grouped",
            "mq_gemm_scratch", "mq_quantize_e4m3", "mq_gemm_e4m3", "mq_weight_e4m3_info",
-           "mq_gemm_e4m3_grouped", "mq_debug_schedule")
+           "mq_gemm_e4m3_grouped", "mq_debug_schedule", "mq_debug_cvt_f16")
 MQ_TRACE_GEMM_CACHED, MQ_TRACE_GEMM_FUSED, MQ_TRACE_DECODE = 1, 2, 3
 
 
@@ -67,6 +67,7 @@ def _load() -> ctypes.CDLL:
         "mq_gemm_auto_grouped": ([_P, ctypes.POINTER(_P), ctypes.c_int, ctypes.POINTER(_P), _I64, _P], ctypes.c_int),
         "mq_debug_schedule": ([_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _I64, _P],
                               ctypes.c_int),
+        "mq_debug_cvt_f16": ([ctypes.c_uint32, _I64, _P, _P], ctypes.c_int),
         "mq_get_m_gate": ([], _I64),
         "mq_set_m_gate": ([_I64], ctypes.c_int),
         "mq_reserve_workspace": ([_I64], ctypes.c_int),
@@ -301,6 +302,13 @@ def mq_debug_schedule(M: int, N: int, K: int, sms: int, path: int = 0, pair_clus
                                     count.value, ctypes.byref(count)), "mq_debug_schedule")
     keys = ("bn", "pair", "split", "full_tiles", "tiles", "units", "grid", "ws_bytes", "kb_align")
     return dict(zip(keys, plan.tolist())), units[: count.value]
+
+
+def mq_debug_cvt_f16(first: int, count: int, out, stream=None) -> None:
+    """out (uint16 / int16 CUDA tensor of >= count elements) <- the f16 bits
+    the decoders' f32 -> f16 step gives for binary32 patterns first ..
+    first + count - 1."""
+    _check(_lib().mq_debug_cvt_f16(first, count, _ptr(out), _stream(stream)), "mq_debug_cvt_f16")
 
 
 def mq_get_m_gate() -> int:

@@ -484,12 +484,17 @@ int gemm_cached_into_scratch(const void *x, mq_handle w, float *y, int64_t M, cu
         return fail(MQ_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
     if (dev != w->device)
         return fail(MQ_ERR_INVALID, "weight was registered on device %d, current device is %d", w->device, dev);
-    const int64_t want = plan_ws_bytes_wanted(M, w->N, w->K, sms, false);
-    if (want > scratch_bytes)
+    // One plan, made as if scratch were unlimited, is both checked against
+    // the scratch size and launched, so the check cannot drift from what the
+    // kernels write.  Single CTAs only (no pair clusters, no 2-SM MMAs).
+    const GemmPlan plan = plan_gemm(M, w->N, w->K, sms, false, INT64_MAX);
+    if (plan.pair != 0 || plan.two_sm != 0)
+        return fail(MQ_ERR_INVALID, "internal: the scratch plan must use single CTAs");
+    if (plan.ws_bytes > scratch_bytes)
         return fail(MQ_ERR_SHAPE,
                     "M=%lld N=%lld K=%lld needs %lld bytes of split-K scratch; the static scratch holds %lld bytes",
-                    (long long)M, (long long)w->N, (long long)w->K, (long long)want, (long long)scratch_bytes);
-    const GemmPlan plan = plan_gemm(M, w->N, w->K, sms, false, scratch_bytes);
+                    (long long)M, (long long)w->N, (long long)w->K, (long long)plan.ws_bytes,
+                    (long long)scratch_bytes);
 
     CUtensorMap tm_x;
     CUresult cr = encode_f16_2d(&tm_x, x, M, w->K, w->K, 64, plan.bn);
@@ -979,6 +984,28 @@ int mq_debug_schedule(int64_t M, int64_t N, int64_t K, int sms, int path, int pa
     plan_out[7] = p.ws_bytes;
     plan_out[8] = p.kb_align;
     *count = mq::schedule_units(p, M, N, K, kstep, units, cap);
+    return MQ_OK;
+}
+
+int mq_debug_cvt_f16(uint32_t first, int64_t count, void *out, void *stream)
+{
+    if (!out)
+        return fail(MQ_ERR_INVALID, "out is NULL");
+    if (count < 0 || (count & 1) || (first & 1u) || count > (int64_t(1) << 32) - int64_t(first))
+        return fail(MQ_ERR_SHAPE, "first=%u count=%lld: need even first and count, first + count <= 2^32", first,
+                    (long long)count);
+    if ((reinterpret_cast<uintptr_t>(out) & 3u) != 0)
+        return fail(MQ_ERR_ALIGN, "out=%p is not 4-byte aligned", out);
+    DevState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc)
+        return rc;
+    if (count == 0)
+        return MQ_OK;
+    cudaError_t e = mq::launch_debug_cvt_f16(first, count, static_cast<uint16_t *>(out),
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "f16 conversion launch");
     return MQ_OK;
 }
 

@@ -395,6 +395,33 @@ cudaError_t launch_t(const void *q, int64_t nblocks, __half *out, int64_t K, int
 
 }  // namespace
 
+namespace {
+
+// The binary32 bit patterns first + i (i < 2 * pairs) through the decoders'
+// own f32 -> f16 step (cvt_f16x2: two values, round to nearest even):
+// out[i] holds the f16 bits of pattern first + 2i (low half) and
+// first + 2i + 1 (high half).  Test hook for that rounding step.
+__global__ void k_debug_cvt_f16(uint32_t first, uint32_t pairs, uint32_t *__restrict__ out)
+{
+    grid_dep_wait();
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
+        const uint32_t b = first + 2u * i;
+        out[i] = cvt_f16x2(f32x2(__uint_as_float(b), __uint_as_float(b + 1u)));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_debug_cvt_f16(uint32_t first, int64_t count, uint16_t *out, cudaStream_t s)
+{
+    const uint32_t pairs = static_cast<uint32_t>(count / 2);
+    const cudaError_t e = launch_kernel(k_debug_cvt_f16, dim3(1216), dim3(256), 0, s, first, pairs,
+                                        reinterpret_cast<uint32_t *>(out));
+    note_launch();
+    return e;
+}
+
 cudaError_t launch_dequant(int type, const void *q, int64_t nblocks, __half *out, int64_t K, int64_t ldo,
                            cudaStream_t s)
 {

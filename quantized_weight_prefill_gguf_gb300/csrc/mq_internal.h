@@ -18,6 +18,11 @@ void note_launch();
 cudaError_t launch_dequant(int type, const void *q, int64_t nblocks, __half *out, int64_t K, int64_t ldo,
                            cudaStream_t s);
 
+// The decoders' f32 -> f16 rounding step on the binary32 patterns
+// first .. first + count - 1 (count even, first even): out[i] = f16 bits of
+// pattern first + i.
+cudaError_t launch_debug_cvt_f16(uint32_t first, int64_t count, uint16_t *out, cudaStream_t s);
+
 // ---------------------------------------------------------------- GEMMs
 // Work decomposition of one GEMM: the output is cut into tiles of 128
 // weight rows (MMA M) x BN tokens (MMA N); tiles [0, full_tiles) run over

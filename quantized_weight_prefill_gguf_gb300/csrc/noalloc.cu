@@ -30,6 +30,8 @@ constexpr int64_t kScratchBytes = int64_t(16) << 20;
 __device__ __align__(256) float g_noalloc_scratch[kScratchBytes / sizeof(float)];
 __device__ __align__(16) unsigned g_noalloc_status;   // bounded-wait timeouts of these calls
 
+__global__ void k_clear_status_bits(unsigned bits) { atomicAnd(&g_noalloc_status, ~bits); }
+
 struct DevPtrs {
     bool ready = false;
     float *scratch = nullptr;
@@ -76,8 +78,12 @@ unsigned noalloc_take_status()
     if (cudaMemcpyFromSymbol(&v, g_noalloc_status, sizeof v) != cudaSuccess)
         return 0;
     if (v != 0) {
-        const unsigned zero = 0;
-        cudaMemcpyToSymbol(g_noalloc_status, &zero, sizeof zero);
+        // Clear only the bits just read, atomically on the device: a bit that
+        // a call still running on another stream sets in the meantime stays
+        // set for the next read.
+        k_clear_status_bits<<<1, 1>>>(v);
+        if (cudaGetLastError() == cudaSuccess)
+            cudaStreamSynchronize(0);
     }
     return v;
 }
