@@ -496,13 +496,25 @@ def e2e_run(mq, torch, weights, handles, xs, ys, stream, steps, flops_step):
 
 def _rotating_time_us(torch, fns, stream, reps=5):
     """Median per-call device time of the calls in `fns`, issued back to back
-    on `stream` (CUDA events around the whole run of calls)."""
+    on `stream` (CUDA events around the whole run of calls).  A sleep kernel
+    ahead of the first event keeps the stream busy while the host enqueues
+    the calls: an event recorded on an idle GPU would start the clock before
+    the host has submitted the first call, adding its launch latency to the
+    run."""
     for fn in fns:
         fn()
     torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for fn in fns:
+        fn()
+    host_s = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    busy_cycles = int(max(50e-6, 2.0 * host_s) * 2.5e9)
     ts = []
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(busy_cycles)
         a.record(stream)
         for fn in fns:
             fn()
