@@ -74,6 +74,8 @@ METRIC = "prefill GEMM TFLOP/s & tok/s per 7B layer at M=2048; % of f16 TC / HBM
 WORKLOAD = "qwen2.5-7b_layer"
 M_TOKENS = 2048
 L2_BYTES = 126 * 1024 * 1024
+NOMINAL_F16_TFLOPS = 2250.0   # dense f16/bf16 tensor rate per GB300, vendor figure
+NOMINAL_HBM_GBS = 7900.0      # HBM3e per GB300, vendor figure
 
 
 def peaks():
@@ -373,6 +375,8 @@ def main():
                 "peak_f16_same_run": f16_peak,
                 "frac_of_f16_same_run": (achieved / f16_peak) if achieved and f16_peak else None,
                 "frac_of_sustained": (achieved / P["bf16_tflops_sustained"]) if achieved else None,
+                "frac_of_nominal": (achieved / NOMINAL_F16_TFLOPS) if achieved else None,
+                "nominal_note": f"{NOMINAL_F16_TFLOPS:.0f} TFLOP/s dense f16 per GB300 (vendor figure, not measured)",
                 "step_frac": value / P["bf16_tflops"],
                 "kernel_share_of_step": share, "kernel_ms_per_step": kern_ms,
                 "launches_per_step": n_launch,
@@ -876,7 +880,8 @@ def registration_decode(mq, torch, stream, weights, qdev, P):
     for h in hs:
         h.release()
     gbs = nbytes / (best["ms"] * 1e-3) / 1e9
-    best.update({"bytes": nbytes, "gbs": gbs, "frac_hbm": gbs / P["hbm_gbs"], "kernel_ms_traced": kern_ms,
+    best.update({"bytes": nbytes, "gbs": gbs, "frac_hbm": gbs / P["hbm_gbs"],
+                 "frac_hbm_nominal": gbs / NOMINAL_HBM_GBS, "kernel_ms_traced": kern_ms,
                  "kernel_gbs_traced": nbytes / (kern_ms * 1e-3) / 1e9 if kern_ms else None,
                  "stream_stayed_busy": best["issue_ms"] < best["busy_ms"],
                  "weights": len(weights),
