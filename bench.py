@@ -21,6 +21,8 @@ Printed: one JSON line with the contract keys plus
                 decoders per format and its GEMM time per configuration;
   e2e           the same metric with host buffers: pinned-host inputs copied
                 in and all outputs copied out inside the timed region;
+  library_f16_layer  context: the same step through cuBLAS (torch.mm) on the
+                same decoded f16 weights, f32 and f16 outputs;
   decode        the registration decoders (mq_register_weight of the 7
                 weights back to back on a busy stream) against HBM bandwidth;
   decode_steady the decoders back to back on the 7B gate/down shapes and
@@ -408,6 +410,8 @@ def main():
 
     if not args.no_extras:
         out["e2e"] = e2e_run(mq, torch, weights, handles, xs, ys, stream, min(args.steps, 50), flops_step)
+        out["library_f16_layer"] = library_layer(mq, torch, stream, weights, qdev, xdev, min(args.steps, 50),
+                                                 flops_step, ms)
         out["small_m"] = small_m_sweep(mq, torch, stream, P)
         out["decode_steady"] = decode_steady(mq, torch, stream, P)
         out["c2_llama3.1-8b_layer"] = llama_layer(mq, torch, stream, P)
@@ -803,6 +807,61 @@ def decode_steady(mq, torch, stream, P):
                                     "frac_hbm": byts / (t_us * 1e-6) / 1e9 / P["hbm_gbs"]}
         del qs, dst
     mq.mq_stream_status()
+    return out
+
+
+def library_layer(mq, torch, stream, weights, qdev, xdev, steps, flops_step, ms_ours):
+    """Context, not a product path: the same layer step through a library
+    GEMM (torch.mm, i.e. cuBLAS) on the same f16 operands -- the weights
+    decoded by mq_dequantize into plain N x K f16 tensors, concatenated per
+    launch group exactly as the library's grouped launches see them -- timed
+    like the step (events around `steps` back-to-back steps after warm-up;
+    the 466 MB of f16 weights per step exceed L2).  Two output types: f32
+    (the library's own output type; torch.mm with out_dtype, where this
+    torch has it) and f16."""
+    w16 = []
+    for w, q in zip(weights, qdev):
+        t = torch.empty((w.N, w.K), dtype=torch.float16, device="cuda")
+        mq.mq_dequantize(w.qtype, q, w.N, w.K, t, stream=stream)
+        w16.append(t)
+    by_name = {w.name: i for i, w in enumerate(weights)}
+    groups = []
+    for grp in LAUNCH_GROUPS:
+        idx = [by_name[n] for n in grp]
+        wt = torch.cat([w16[i] for i in idx], 0) if len(idx) > 1 else w16[idx[0]]
+        groups.append((xdev[weights[idx[0]].K], wt))
+    del w16
+    out = {"ms_per_step_ours": ms_ours,
+           "note": "cuBLAS through torch.mm on the decoded f16 weights, one GEMM per launch group "
+                   "(q|k|v, o, gate|up, down); a comparison only, never the library's path"}
+    for label, dt in (("f32_out", torch.float32), ("f16_out", torch.float16)):
+        ys = [torch.empty((x.shape[0], wt.shape[0]), dtype=dt, device="cuda") for x, wt in groups]
+
+        def step():
+            for (x, wt), y in zip(groups, ys):
+                if dt == torch.float32:
+                    torch.mm(x, wt.t(), out_dtype=torch.float32, out=y)
+                else:
+                    torch.mm(x, wt.t(), out=y)
+        try:
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize()
+        except (RuntimeError, TypeError) as e:
+            out[label] = {"unavailable": str(e).splitlines()[0][:160]}
+            continue
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / steps
+        out[label] = {"ms_per_step": t, "tflops": flops_step / (t * 1e-3) / 1e12,
+                      "ours_over_library": t / ms_ours}
+        del ys
+    del groups
+    torch.cuda.empty_cache()
     return out
 
 

@@ -44,6 +44,9 @@
  *                 of a cluster share each token tile).
  *   MQ_2SM=0      256-token tiles as multicast CTA pairs instead of 2-SM MMAs
  *                 (tcgen05.mma.cta_group::2, the default).
+ *   MQ_TMA_Y=0    cached / e4m3 GEMMs store whole output tiles with plain
+ *                 stores instead of TMA stores of staged boxes (default on
+ *                 where Y is 16-byte aligned and N % 4 == 0).
  *   MQ_SPLITK=0   no split-K tail (default on).
  *   MQ_BN=32|64|128|256   force the cached GEMM's token-tile width.
  *   MQ_PDL=0      launch without programmatic dependent launch (default on;
@@ -400,7 +403,8 @@ int mq_debug_cvt_f16(uint32_t first, int64_t count, void *out, void *stream);
  * Result: within the GEMM tolerance of mq_gemm, not bit for bit.  It runs
  * the single-CTA plan (no CTA pairs, no 2-SM MMAs) with its split-K tail
  * bounded by the scratch below, so its summation order can differ; the
- * tuning switches MQ_SPLITK, MQ_BN, MQ_PAIR and MQ_2SM do not apply to it.
+ * tuning switches MQ_SPLITK, MQ_BN, MQ_PAIR and MQ_2SM do not apply to it
+ * (MQ_TMA_Y does: the output path is the same kernel's).
  *
  * Its split-K scratch is one 16 MiB file-scope device array, which every GPU
  * that loads this library holds until the process exits.  A call whose split

@@ -362,6 +362,8 @@ int run_gemm_group(const void *x, const mq_handle *ws, float *const *ys, int cou
     // kernel's bounded waits run out (about 1 s), it exits cleanly and
     // mq_stream_status() reports MQ_ERR_DEVICE.
     a.stall_producer = env_int("MQ_INJECT_PRODUCER_STALL", 0) != 0 ? 1 : 0;
+    if (!fused)
+        mq::set_output_maps(maps, a);
     cudaError_t e = fused ? mq::launch_gemm_fused(tm_x, raw, a, plan, s)
                           : mq::launch_gemm_cached(maps, tm_x, a, plan, s);
     if (e != cudaSuccess)
@@ -418,7 +420,9 @@ typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32
 namespace {
 
 CUresult encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, int esize, const void *base, int64_t rows,
-                   int64_t cols, int64_t ld, int box_cols, int box_rows)
+                   int64_t cols, int64_t ld, int box_cols, int box_rows,
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+                   CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
 {
     static PFN_encodeTiled fn = nullptr;
     if (!fn) {
@@ -435,10 +439,31 @@ CUresult encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, int esize, const
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+              swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 }  // namespace
+
+CUresult encode_f32_out_2d(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows)
+{
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, cols, ld, 32, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+}
+
+void set_output_maps(WMaps &maps, GemmArgs &a)
+{
+    a.y_tma = 0;
+    if (env_int("MQ_TMA_Y", 1) == 0)
+        return;
+    for (int g = 0; g < a.groups; ++g) {
+        const uintptr_t b = reinterpret_cast<uintptr_t>(a.g_y[g]);
+        if ((b & 15u) != 0 || (a.g_N[g] & 3) != 0)
+            return;
+        if (encode_f32_out_2d(&maps.y[g], a.g_y[g], a.M, a.g_N[g], a.g_N[g], kYBoxRows) != CUDA_SUCCESS)
+            return;
+    }
+    a.y_tma = 1;
+}
 
 CUresult encode_f16_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
                        int box_rows)
@@ -524,6 +549,7 @@ int gemm_cached_into_scratch(const void *x, mq_handle w, float *y, int64_t M, cu
     a.g_N[0] = w->N;
     WMaps maps{};
     maps.m[0] = w->tm_cache;
+    set_output_maps(maps, a);
     e = launch_gemm_cached(maps, tm_x, a, plan, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "cached GEMM launch");
@@ -1113,6 +1139,7 @@ int run_e4m3_group(const void *x8, const float *x_scale, const mq_handle *ws, fl
     }
     a.g_tile0[count] = nt;
     a.n_tiles = nt;
+    mq::set_output_maps(maps, a);
     const int64_t tr = trace_begin(s, MQ_TRACE_GEMM_CACHED, w->type, M, n_total, w->K);
     cudaError_t e = mq::launch_gemm_e4m3(maps, tm_x, a, plan, s);
     if (e != cudaSuccess)

@@ -59,7 +59,7 @@ template <int BN> struct Cfg {
     static constexpr int kBBytes = BN * kBK * 2;
     static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
     static constexpr int kTmemCols = 2 * BN;   // two accumulators
-    static constexpr int kSmem = 1024 + kStages * (kABytes + kBBytes) + 256;
+    static constexpr int kSmem = 1024 + kStages * (kABytes + kBBytes) + kYStageBytes + 256;
 };
 
 // The kernel body: F8 selects e4m3 operands (K step kBK8, kind::f8f6f4,
@@ -74,7 +74,8 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
     uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = base;
     uint8_t *sB = base + C::kStages * kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kBBytes);
+    float *sY = reinterpret_cast<float *>(sB + C::kStages * C::kBBytes);   // staged output boxes
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kBBytes + kYStageBytes);
     uint64_t *empty = full + C::kStages;
     uint64_t *tfull = empty + C::kStages;
     uint64_t *tempty = tfull + 2;
@@ -255,7 +256,7 @@ __device__ __forceinline__ void gemm_body(const WMaps &tm_w, const CUtensorMap &
         }
     } else {
         // ---------------- epilogue: warps 2..5 own TMEM lane quarters 2,3,0,1
-        epilogue_role<BN, 2, 1, F8>(a, tmem, tfull, tempty, abort_flag, warp, lane);
+        epilogue_role<BN, 2, 1, F8, true>(a, tmem, tfull, tempty, abort_flag, warp, lane, 1, -1, tm_w.y, sY);
     }
 
     tc_fence_before();
@@ -312,7 +313,7 @@ template <int BN, bool F8 = false> struct Cfg2 {
     static constexpr int kStageA = kSub * kABytes;
     static constexpr int kStageB = kSub * kHalfB;
     static constexpr int kTmemCols = kTwoSmAccs * BN;
-    static constexpr int kSmem = 1024 + kStages * (kStageA + kStageB) + 512;
+    static constexpr int kSmem = 1024 + kStages * (kStageA + kStageB) + kYStageBytes + 512;
 };
 
 template <int BN, bool F8>
@@ -324,7 +325,8 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
     uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = base;
     uint8_t *sB = base + C::kStages * C::kStageA;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kStageB);
+    float *sY = reinterpret_cast<float *>(sB + C::kStages * C::kStageB);   // staged output boxes
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kStageB + kYStageBytes);
     uint64_t *empty = full + C::kStages;
     uint64_t *tfull = empty + C::kStages;
     uint64_t *tempty = tfull + 2;
@@ -515,7 +517,7 @@ __device__ __forceinline__ void gemm_body_2sm(const WMaps &tm_w, const CUtensorM
         }
     } else {
         // ---------------- epilogue: warps 2..5, this CTA's 128 rows of D
-        epilogue_role<BN, kTwoSmAccs, 1, F8>(a, tmem, tfull, tempty, abort_flag, warp, lane, 1, 0);
+        epilogue_role<BN, kTwoSmAccs, 1, F8, true>(a, tmem, tfull, tempty, abort_flag, warp, lane, 1, 0, tm_w.y, sY);
     }
 
     tc_fence_before();

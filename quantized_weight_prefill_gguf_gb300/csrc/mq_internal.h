@@ -63,6 +63,8 @@ struct GemmArgs {
     int stall_producer;  // failure-injection hook: the weight producer issues nothing, so the
                          // consumers' bounded waits run out (tests of the timeout path)
     int pair;                       // CTAs run in clusters of two (see tile_coords)
+    int y_tma;                      // cached/e4m3 GEMMs: whole-tile outputs leave by TMA stores
+                                    // through WMaps::y (set only when every member's map exists)
     const float *x_scale;           // 8-bit path: per-token scale of X [M]
     const float *g_wscale[kMaxGroup];  // 8-bit path: per-row scale of each member's weight
     int groups;                     // members of the group (1 for a single weight)
@@ -81,9 +83,15 @@ __host__ __device__ inline int group_of(const GemmArgs &a, int nt)
     return g;
 }
 
-// f16-cache tensor maps of the members of a group (one for a single weight).
+// Tokens per output box that the cached/e4m3 epilogue stores by TMA.
+constexpr int kYBoxRows = 16;
+
+// Tensor maps of the members of a group (one for a single weight): the
+// f16 weight caches (m) and, for GEMMs launched with y_tma, the f32 outputs
+// (y: [M, N_g], box 16 tokens x 32 rows, no swizzle).
 struct WMaps {
     CUtensorMap m[kMaxGroup];
+    CUtensorMap y[kMaxGroup];
 };
 
 // Raw-weight tensor maps of a weight whose rows start on block boundaries
@@ -189,6 +197,15 @@ CUresult encode_f16_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t
                        int box_cols, int box_rows);
 
 // The same for a byte matrix (e4m3 codes): ld in bytes.
+// Output map of a cached/e4m3 GEMM: f32 Y [rows = M, cols = N], row stride
+// ld floats, box box_rows x 32.  Needs a 16-byte aligned base and ld % 4 == 0.
+CUresult encode_f32_out_2d(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows);
+
+// Fill maps.y and set a.y_tma for the members' outputs a.g_y / a.g_N (M
+// tokens) when every output allows a TMA store (16-byte aligned base, N % 4
+// == 0) and MQ_TMA_Y is not 0; otherwise a.y_tma = 0 (plain stores).
+void set_output_maps(WMaps &maps, GemmArgs &a);
+
 CUresult encode_u8_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld,
                       int box_cols, int box_rows);
 
