@@ -88,7 +88,7 @@ constexpr int kYBoxRows = 16;
 
 // Tensor maps of the members of a group (one for a single weight): the
 // f16 weight caches (m) and, for GEMMs launched with y_tma, the f32 outputs
-// (y: [M, N_g], box 16 tokens x 32 rows, no swizzle).
+// (y: [M, N_g], box 16 tokens x 128 rows, no swizzle).
 struct WMaps {
     CUtensorMap m[kMaxGroup];
     CUtensorMap y[kMaxGroup];
@@ -198,7 +198,7 @@ CUresult encode_f16_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t
 
 // The same for a byte matrix (e4m3 codes): ld in bytes.
 // Output map of a cached/e4m3 GEMM: f32 Y [rows = M, cols = N], row stride
-// ld floats, box box_rows x 32.  Needs a 16-byte aligned base and ld % 4 == 0.
+// ld floats, box box_rows x 128.  Needs a 16-byte aligned base and ld % 4 == 0.
 CUresult encode_f32_out_2d(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows);
 
 // Fill maps.y and set a.y_tma for the members' outputs a.g_y / a.g_N (M

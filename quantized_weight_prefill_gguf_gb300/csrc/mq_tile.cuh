@@ -106,20 +106,27 @@ __device__ __forceinline__ UnitWalk unit_walk(const GemmArgs &a)
 // which counts the epilogue warps of both CTAs.
 //
 // TMA_Y with a.y_tma set: whole-tile outputs leave through TMA stores
-// instead of st.global.  Each warp stages a box of 32 weight rows x kYRows
-// tokens in shared memory as [token][row] (the lanes' writes hit 32
-// consecutive words) and one lane stores it through member g's map ymaps[g]
-// (f32 [M, N_g], box kYRows x 32), which clips rows past N_g and tokens past
-// M.  Two boxes per warp alternate, so a box is rewritten only after the
-// store issued two boxes earlier has read it; the role waits for all its
-// stores before it returns.  With plain stores the 2-SM GEMM's tensor pipe
-// was busy 85 % of its active cycles: on the 7B gate|up GEMM (2048 x 37888
-// x 3584) a timing copy without the output stores took 297 us against
-// 320 us with them, i.e. the stores overlapping the next tile's main loop
-// starved the MMAs; the staged bulk stores take it to 309 us.
+// instead of st.global.  The four epilogue warps stage a box of the tile's
+// 128 weight rows x kYRows tokens in shared memory as [token][row] (a warp's
+// writes hit 32 consecutive words) and one thread (lane 0 of the warp with
+// q = 0) stores it through member g's map ymaps[g] (f32 [M, N_g], box
+// kYRows x 128), which clips rows past N_g and tokens past M.  Two boxes
+// alternate, so a box is rewritten only after the store issued two boxes
+// earlier has read it; the storing thread waits for all its stores before
+// the role returns.  The warps meet on named barrier 1 (128 threads) twice
+// per box; every condition that skips a box or leaves the unit loop is the
+// same for all four warps (they wait on the same accumulator phase, which
+// cannot advance before all four have released it, and the box position
+// depends only on the unit and the column), so no warp waits there alone.
+// With plain stores the 2-SM GEMM's tensor pipe was busy 85 % of its active
+// cycles: on the 7B gate|up GEMM (2048 x 37888 x 3584) a timing copy without
+// the output stores took 297 us against 320 us with them -- stores
+// overlapping the next tile's main loop starved the MMAs.  Per-warp boxes of
+// 32 rows brought it to 309 us and one 128-row box per kYRows tokens (four
+// times fewer store operations) a little further.
 constexpr int kYRows = kYBoxRows;   // tokens per staged output box
-constexpr int kYBufs = 2;    // staged boxes per epilogue warp
-constexpr int kYStageBytes = 4 * kYBufs * 32 * kYRows * 4;   // four warps' boxes
+constexpr int kYBufs = 2;           // staged boxes, used in turn
+constexpr int kYStageBytes = kYBufs * kTileRows * kYRows * 4;
 
 template <int BN, int NACC = 2, int NPART = 1, bool SCALED = false, bool TMA_Y = false>
 __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, uint64_t *tfull, uint64_t *tempty,
@@ -188,23 +195,24 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
                 }
             }
             if (TMA_Y && kCols == 32 && ui.part < 0 && a.y_tma) {
-                const int64_t nw0 = n - lane;   // the warp's first weight row in member g
+                const int64_t nt0 = n - row;   // the tile's first weight row in member g
+                const bool storer = q == 0 && lane == 0;
 #pragma unroll
                 for (int h = 0; h < 32 / kYRows; ++h) {
                     const int64_t mh = m0 + c + h * kYRows;
-                    if (nw0 >= Ng || mh >= a.M)   // box entirely past the output: nothing to store
+                    if (mh >= a.M)   // box entirely past the last token: nothing to store
                         continue;
-                    float *box = ystage + (q * kYBufs + ybuf) * (32 * kYRows);
-                    if (lane == 0)
+                    float *box = ystage + ybuf * (kTileRows * kYRows);
+                    if (storer)
                         bulk_wait_group_read<kYBufs - 1>();
-                    __syncwarp();
+                    named_barrier_sync(1, 128);
 #pragma unroll
                     for (int j = 0; j < kYRows; ++j)
-                        box[j * 32 + lane] = __uint_as_float(r[h * kYRows + j]);
+                        box[j * kTileRows + row] = __uint_as_float(r[h * kYRows + j]);
                     fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&ymaps[g], box, static_cast<int32_t>(nw0), static_cast<int32_t>(mh));
+                    named_barrier_sync(1, 128);
+                    if (storer) {
+                        tma_store_2d(&ymaps[g], box, static_cast<int32_t>(nt0), static_cast<int32_t>(mh));
                         bulk_commit_group();
                     }
                     ybuf = ybuf + 1 == kYBufs ? 0 : ybuf + 1;
