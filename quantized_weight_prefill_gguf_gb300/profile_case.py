@@ -7,7 +7,11 @@ Cases: cached (mq_gemm), fused (mq_gemm_fused), decode (mq_dequantize),
 e4m3 (mq_gemm_e4m3 on activations quantized once before), quant
 (mq_quantize_e4m3 of the M x K activations).  --group G (cached, fused): G
 weights of the shape in one mq_gemm_grouped / mq_gemm_fused_grouped call.
-Inputs are the seeded synthetic blocks of the given shape.  Prints the
+--library (cached, one weight): after the library's calls, the same GEMM
+through cuBLAS (torch.mm with an f32 output) on the weight decoded to f16 by
+mq_dequantize, --reps times, for a side-by-side capture of the two kernels;
+a comparison only.  Inputs are the seeded synthetic blocks of the given
+shape.  Prints the
 device time of each call from the library's trace events (not valid under a
 profiler, which serialises and replays kernels).
 """
@@ -33,7 +37,10 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--group", type=int, default=1)
+    ap.add_argument("--library", action="store_true")
     args = ap.parse_args(argv)
+    if args.library and (args.case != "cached" or args.group != 1):
+        ap.error("--library applies to --case cached with one weight")
 
     qtype = TYPES[args.type]
     g = synth.rng(args.seed)
@@ -78,6 +85,15 @@ def main(argv=None):
     for r in mq.mq_trace_records():
         print(f"{args.case} {args.type} M={args.M} N={args.N}x{args.group} K={args.K}: "
               f"{r['ms_main'] * 1e3:.1f} us (+ reduce {r['ms_aux'] * 1e3:.1f} us)")
+    if args.library:
+        w16 = torch.empty((args.N, args.K), dtype=torch.float16, device="cuda")
+        mq.mq_dequantize(qtype, q, args.N, args.K, w16)
+        y_lib = torch.empty_like(y)
+        for _ in range(args.reps):
+            torch.mm(x, w16.t(), out_dtype=torch.float32, out=y_lib)
+        torch.cuda.synchronize()
+        print(f"library (torch.mm, f32 out) on the same f16 weight: max |difference| "
+              f"{float((y - y_lib).abs().max()):.3g}")
     mq.mq_trace_enable(False)
 
 
