@@ -1026,7 +1026,7 @@ def q8_pair(mq, torch, stream, P):
     2-byte aligned; K = 18944 and 3584 are not multiples of 1024, so the
     caches are not padded).  Decode through mq_register_weight (busy-stream
     sequence) and mq_dequantize back to back; GEMMs through the cached path,
-    the fused path and the M gate at M in {1, 8, 32, 128, 256, 512, 1024}
+    the fused path and the M gate at M in {1, 8, 32, 128, 129, 192, 256, 512, 1024}
     (M = 128 and 1024 are the configuration's own), rotating copies."""
     clocks = ClockSampler(0)
     clocks.start()
@@ -1046,7 +1046,7 @@ def q8_pair(mq, torch, stream, P):
     rows = []
     for w in weights:
         x_all = torch.from_numpy(xs[w.K]).cuda()
-        rows += _paths_rotating(mq, torch, stream, P, w, x_all, [1, 8, 32, 128, 256, 512, 1024],
+        rows += _paths_rotating(mq, torch, stream, P, w, x_all, [1, 8, 32, 128, 129, 192, 256, 512, 1024],
                                 ("fused", "cached", "auto"))
     cross = {}
     for w in weights:

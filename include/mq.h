@@ -39,7 +39,8 @@
  *
  * Environment switches (read on every call unless noted; tuning and
  * diagnostics only, never needed for correct results):
- *   MQ_M_GATE=n   mq_gemm_auto's token threshold (default 256).
+ *   MQ_M_GATE=n   mq_gemm_auto's token threshold (default 129: the fused path
+ *                 up to M = 128, the measured crossover).
  *   MQ_PAIR=0     cached / e4m3 GEMMs without CTA pairs (default on: two CTAs
  *                 of a cluster share each token tile).
  *   MQ_2SM=0      256-token tiles as multicast CTA pairs instead of 2-SM MMAs
@@ -271,9 +272,11 @@ int mq_gemm_auto_grouped(const void *x, const mq_handle *w, int count, float *co
  * cached otherwise ("ggml-cuda: GEMM weight row padding ...", Summary: the
  * f16 path is a large-batch win; the threshold is a token count per call).
  * The gate is mq_get_m_gate(); environment variable MQ_M_GATE overrides it.
- * Default 256: measured on GB300 with the 7B gate (Q4_K 18944x3584) and down
- * (Q6_K 3584x18944) shapes, calls back to back over weights larger than L2,
- * the fused path is faster up to M = 128 and the cached path from M = 256.
+ * Default 129: measured on GB300, calls back to back over weights larger than
+ * L2, the fused path is faster up to M = 128 and the cached path from M = 129
+ * on the 7B gate, down and o shapes, the Q8_0 pair and the Llama-3.1-8B gate
+ * (the fused path's token tiles stop at 128, so past that it decodes each
+ * weight tile once per token tile).
  */
 int mq_gemm_auto(const void *x, mq_handle w, float *y, int64_t M, void *stream);
 

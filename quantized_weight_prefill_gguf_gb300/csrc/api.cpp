@@ -238,14 +238,18 @@ int64_t env_int(const char *name, int64_t dflt)
 }
 
 // Token count at and above which mq_gemm_auto takes the cached path: the
-// measured fused/cached crossover of the 7B gate and down shapes on GB300
-// (fused faster up to M = 128, cached from M = 256).
+// measured fused/cached crossover on GB300.  The fused path's token tiles
+// stop at 128, so from M = 129 on it decodes every weight tile once per
+// token tile; back to back, the fused path is faster up to M = 128 and the
+// cached path from M = 129 on every shape measured (7B gate, down and o, the
+// Q8_0 pair, the Llama-3.1-8B gate; e.g. 7B down at M = 160: 37.0 us cached
+// against 54.7 us fused).
 int64_t current_gate()
 {
     int64_t g = g_gate.load();
     if (g > 0)
         return g;
-    return env_int("MQ_M_GATE", 256);
+    return env_int("MQ_M_GATE", 129);
 }
 
 // Whether 256-token tiles run as 2-SM MMAs (tcgen05.mma.cta_group::2,

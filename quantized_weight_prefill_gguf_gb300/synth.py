@@ -210,7 +210,7 @@ WORKLOADS = {
     "more_formats": (MORE_FORMATS, [32, 2048]),
     "float_layer": (FLOAT_LAYER, [512]),
     "small_m_sweep": ([w for w in QWEN25_7B if w[0] in ("gate", "up", "down")],
-                      [1, 8, 32, 128, 256, 512, 2048]),
+                      [1, 8, 32, 128, 129, 192, 256, 512, 2048]),
 }
 
 

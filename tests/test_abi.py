@@ -63,6 +63,9 @@ def test_host_validation_without_device(lib):
     assert lib.mq_gemm(ctypes.c_void_p(16), ctypes.c_void_p(0x1234), ctypes.c_void_p(16), 8, None) == -1
     assert lib.mq_release_weight(ctypes.c_void_p(0x1234)) == -1
     assert lib.mq_set_m_gate(0) == -1
+    # the default gate is the measured fused/cached crossover (fused up to M = 128)
+    if not os.environ.get("MQ_M_GATE"):
+        assert lib.mq_get_m_gate() == 129
     assert lib.mq_reserve_workspace(-1) == -1
     # grouped entry points: null arrays, count out of range, stale member handles
     P = ctypes.c_void_p
