@@ -6,6 +6,8 @@ f32, so Y must equal the oracle's decoded W^T -- the same f16 values the
 cache holds ("05 · 8p", section 3.3: fused and cached must round the same
 way).  The rest compares Y with the oracle's f64 GEMM within tolerance.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -153,3 +155,30 @@ def test_raw_paths_agree(orc, qtype, N, K, monkeypatch):
     for h in (h_tma, h_bulk):
         y = run(mq.mq_gemm_fused, x, h, K, N)
         assert np.array_equal(y, W.T)
+
+
+def test_default_gate_boundary(orc):
+    """With the default gate (the measured crossover, 129 tokens) mq_gemm_auto
+    launches the fused kernel at M = 128 and the cached kernel at M = 129,
+    read from the launch trace; both results within tolerance."""
+    torch = torch_cuda()
+    mq = _mq()
+    if os.environ.get("MQ_M_GATE"):
+        pytest.skip("MQ_M_GATE overrides the default gate")
+    assert mq.mq_get_m_gate() == 129
+    g = synth.rng(17)
+    N, K = 384, 1024
+    data = synth.weight_bytes(g, synth.Q4_K, N, K)
+    h = mq.mq_register_weight(synth.Q4_K, dev(data), N, K)
+    W = orc.decode_matrix(synth.Q4_K, data, N, K)
+    x = synth.activations(g, 129, K)
+    for M, want in ((128, mq.MQ_TRACE_GEMM_FUSED), (129, mq.MQ_TRACE_GEMM_CACHED)):
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        mq.mq_trace_enable(True)
+        mq.mq_gemm_auto(dev(x[:M]), h, y, M)
+        mq.mq_stream_status()
+        kinds = {r["kind"] for r in mq.mq_trace_records()}
+        mq.mq_trace_enable(False)
+        assert kinds == {want}, f"M={M}: trace kinds {kinds}"
+        assert_gemm_close(y.cpu().numpy(), orc.gemm_f64(x[:M].view(np.uint16), W), f"auto M={M}")
+    h.release()
