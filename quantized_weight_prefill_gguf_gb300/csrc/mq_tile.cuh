@@ -159,6 +159,8 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &a, uint32_t tmem, 
         constexpr int kCols = BN < 32 ? BN : 32;   // columns per TMEM load
 #pragma unroll 1
         for (int c = 0; c < BN; c += kCols) {
+            if (m0 + c >= a.M)   // the rest of the tile's columns are past the last token: nothing
+                break;           // reads them (the reduce skips them too); same for all four warps
             uint32_t r[32];
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * NPART * BN + c);
