@@ -69,7 +69,20 @@ namespace {
 constexpr int kDecodeWarp0 = 8;
 constexpr int kDecodeWarps = 8;                         // 8 or 16
 constexpr int kThreadsF = (kDecodeWarp0 + kDecodeWarps) * 32;
-constexpr int kStepsPerThread = 16 / kDecodeWarps;      // K steps of a chunk per decoder thread
+
+// Decoder groups: with two, the decoder warps split into two groups of four
+// (one warp per TMEM lane quarter) that take alternate chunks, each thread
+// decoding all four K steps of its row; with one, all eight decode every
+// chunk, two K steps per thread.  Measured back to back (rotating copies of
+// an 18944 x 3584 weight, and the 3584 x 18944 Q6_K one): at tiles of up to 32
+// tokens two groups are 2-6 % faster for every format but Q6_K (Q4_K at
+// M = 32: 18.30 -> 17.56 us; Q5_K 21.69 -> 20.44; Q5_0 18.96 -> 17.82); at
+// 128-token tiles and for Q6_K they are as fast or slower (Q6_K down, M = 32:
+// 23.8 -> 25.3 us).
+__host__ __device__ constexpr int decoder_groups(int qt, int bn)
+{
+    return (bn <= 32 && qt != 14) ? 2 : 1;
+}
 constexpr int kChunkSteps = 4;               // K steps (of 64) per raw stage: 256 K elements
 constexpr int kMaxRaw = 8, kMaxStages = 3;
 // MMA issuers: two (warps 1 and 3, on different SM sub-partitions) each
@@ -449,6 +462,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     constexpr int S = a_stages_for(BN);               // A and X stages (one ring of chunk slots)
     static_assert(BN <= 128, "fused tiles stop at 128 tokens");
     constexpr int kIssuers = issuers_for(BN);
+    constexpr int kGroups = decoder_groups(QT, BN);
     constexpr uint32_t kACol0 = a_col0_for(BN);
     static_assert(kNAcc * kIssuers * BN <= static_cast<int>(kACol0) && kACol0 + S * kAStageCols <= kTmemCols,
                   "TMEM budget");
@@ -477,11 +491,11 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     if (threadIdx.x == 0) {
         for (int r = 0; r < R; ++r) {
             mbar_init(&raw_full[r], 1);
-            mbar_init(&raw_empty[r], kDecodeWarps);
+            mbar_init(&raw_empty[r], kDecodeWarps / kGroups);
         }
         for (int s = 0; s < S; ++s) {
             mbar_init(&x_full[s], 1);
-            mbar_init(&ready[s], kDecodeWarps + 1);
+            mbar_init(&ready[s], kDecodeWarps / kGroups + 1);
             mbar_init(&done[s], kIssuers);
         }
         for (int i = 0; i < kNAcc; ++i) {
@@ -713,13 +727,18 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         epilogue_role<BN, kNAcc, kIssuers>(a, tmem, tfull, tempty, abort_flag, warp, lane, kChunkSteps / kIssuers);
     } else if (warp >= kDecodeWarp0) {
         // ---------------- decoders: warp w holds weight rows 32*(w%4) .. +31
-        // (the TMEM lanes it may access) and kStepsPerThread K steps from
-        // j0 = kStepsPerThread*((w-8)/4) of every chunk: thread (row, j0)
-        // writes the f16 of its row for those steps into TMEM lane `row`,
-        // columns 32*j0 .. of the chunk's A stage.
+        // (the TMEM lanes it may access); group grp = dw / kWG decodes the
+        // chunks c with c % kGroups == grp, and in them kSPT K steps from
+        // j0 = kSPT*((dw % kWG)/4): thread (row, j0) writes the f16 of its row
+        // for those steps into TMEM lane `row`, columns 32*j0 .. of the
+        // chunk's A stage.
         const int dw = warp - kDecodeWarp0;
         const int row = (warp & 3) * 32 + lane;
-        const int j0 = kStepsPerThread * (dw >> 2);
+        constexpr int kWG = kDecodeWarps / kGroups;   // warps decoding one chunk
+        constexpr int kSPT = kChunkSteps * 4 / kWG;   // K steps per thread per chunk
+        const int j0 = kSPT * ((dw % kWG) >> 2);
+        const int grp = dw / kWG;
+        int cc = 0;
         const uint32_t lane_base = static_cast<uint32_t>(row & ~31) << 16;
         // shared-memory row of this weight row inside a raw stage
         const int srow = TMA_RAW ? (row % g) * rows_per_class + row / g : row;
@@ -749,6 +768,19 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             }
             for (int kb = ui.kb0; ok && kb < ui.kb1; kb += kChunkSteps) {
                 const int steps = ui.kb1 - kb < kChunkSteps ? ui.kb1 - kb : kChunkSteps;
+                if (kGroups > 1 && (cc++ % kGroups) != grp) {   // the other group's chunk
+                    if (TMA_RAW)
+                        ob += kChunkRowBytes;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    if (++r == R) {
+                        r = 0;
+                        rph ^= 1u;
+                    }
+                    continue;
+                }
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&raw_full[r], rph, abort_flag, a.status) &&
                                                  mbar_wait_bounded(&done[s], ph ^ 1u, abort_flag, a.status))) {
                     ok = false;
@@ -760,7 +792,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 if (TMA_RAW && steps == kChunkSteps) {
                     const uint32_t blk = raw_row + ((mis + ob) & 15u);
 #pragma unroll
-                    for (int jj = 0; jj < kStepsPerThread; ++jj)
+                    for (int jj = 0; jj < kSPT; ++jj)
                         decode_step<QT>(blk, j0 + jj, a_col + 32 * jj);
                     ob += kChunkRowBytes;
                 } else {
@@ -770,7 +802,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                         valid ? row_span<QT>(n, a.K, static_cast<int64_t>(kb) * kBK, static_cast<int64_t>(steps) * kBK).s0
                               : 0;
 #pragma unroll 1
-                    for (int j = j0; j < j0 + kStepsPerThread && j < steps; ++j) {
+                    for (int j = j0; j < j0 + kSPT && j < steps; ++j) {
 #pragma unroll 1
                         for (int h = 0; h < 2; ++h) {
                             uint4 out[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
