@@ -43,16 +43,19 @@
 //               stage; lane 1 announces each slot's landed activations.
 //   warps 4-7   epilogue (TMEM -> Y / split-K workspace; sums the partial
 //               accumulators in a fixed order).
-//   warps 8-15  decoders: thread (row, pair of K steps) turns 128 raw
-//               elements of one weight row per chunk into f16 and stores them
-//               with tcgen05.st into its row's TMEM lane.  Eight warps keep
-//               the integer pipe busy; more of them take issue slots from
-//               the MMA issuers (measured: ~86 cycles per MMA next to 8 busy
-//               warps, ~220 next to 30).
+//   warps 8-15  decoders: each thread turns the raw elements of one weight
+//               row into f16 and stores them with tcgen05.st into its row's
+//               TMEM lane -- at tiles of up to 32 tokens (all formats but
+//               Q6_K) as two groups of four warps on alternate chunks, four
+//               K steps (256 elements) per thread; otherwise all eight warps
+//               on every chunk, two K steps (128 elements) per thread.  Eight
+//               warps keep the integer pipe busy; more of them take issue
+//               slots from the MMA issuers (measured: ~86 cycles per MMA next
+//               to 8 busy warps, ~220 next to 30).
 // Chunk slots: A stage s (TMEM) and X stage s (shared memory) form one slot;
-// `ready[s]` completes when the decoder warps have written A and a second
-// thread of warp 2 has seen the slot's activations land; `done[s]` (an MMA
-// commit) frees both.
+// `ready[s]` completes when the warps that decode the chunk have written A
+// and a second thread of warp 2 has seen the slot's activations land;
+// `done[s]` (an MMA commit) frees both.
 #include <cstdint>
 #include <cuda_runtime.h>
 
