@@ -62,6 +62,38 @@ def test_tma_store_matches_plain_stores(qtype, N, K, M):
     h.release()
 
 
+@pytest.mark.parametrize("qtype,N,K,M", [
+    (synth.Q8_0, 132, 1024, 300),   # a 128-row box cut at row 132
+    (synth.Q4_0, 4, 1024, 257),     # a 4-row weight: one box, 124 rows clipped
+])
+def test_tma_store_partial_row_tiles(orc, qtype, N, K, M):
+    """Whole tiles (split-K off, so the few tiles are not split over K) whose
+    last 128-row box runs past N: the TMA store must clip at row N, equal the
+    plain stores bit for bit and match the oracle."""
+    torch = torch_cuda()
+    mq = _mq()
+    g = synth.rng(N + M)
+    data = synth.weight_bytes(g, qtype, N, K)
+    h = mq.mq_register_weight(qtype, dev(data), N, K)
+    xh = synth.activations(g, M, K)
+    x = dev(xh)
+    old = os.environ.get("MQ_SPLITK")
+    os.environ["MQ_SPLITK"] = "0"
+    try:
+        y_tma = _with_tma_y(True, lambda: _run(torch, mq, x, h, M, N))
+        y_plain = _with_tma_y(False, lambda: _run(torch, mq, x, h, M, N))
+    finally:
+        if old is None:
+            del os.environ["MQ_SPLITK"]
+        else:
+            os.environ["MQ_SPLITK"] = old
+    assert np.all(np.isfinite(y_tma))
+    assert np.array_equal(y_tma.view(np.uint32), y_plain.view(np.uint32))
+    ref = orc.gemm_f64(xh.view(np.uint16), orc.decode_matrix(qtype, data, N, K))
+    assert_gemm_close(y_tma, ref, f"{synth.TYPE_NAME[qtype]} N={N} M={M}, TMA-stored")
+    h.release()
+
+
 def test_grouped_tma_store_matches_plain_and_oracle(orc):
     """Two members in one grouped launch (each with its own output map); the
     second member is also held against the f64 oracle on sampled outputs."""
